@@ -1,0 +1,439 @@
+"""Benchmark of the prefill-only AI.IF / AI_JOIN hot path on GB300.
+
+One step = one pass of the whole path over one batch: the cascade attention over every
+suffix token of the workload, then the restricted head (RMSNorm + 8 columns + argmax) on
+the last token of every suffix. Default workload: the Qwen3-4B-shaped join (8 anchors of
+1,024 tokens, 4,144 suffixes each, suffix length U[8, 24], 32 query / 8 KV heads,
+d = 128; hidden size 2,560 for the head). Inputs are synthetic and seeded and already
+resident in HBM; they are larger than L2, so L2 is not flushed between steps.
+
+Prints ONE JSON line (metric: suffix tokens per second). `--impl reference` times the
+float64 CPU oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "suffix tokens/sec (cascade prefill attn) and % of GB300 BF16 tensor/HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="join", choices=["join", "ragged", "fp8_long"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def attention_flops(layout, hq, d) -> float:
+    """4 d Hq sum_s sum_{i < l_s} (L_a + i + 1): only visible (query, key) pairs count."""
+    la = layout.anchor_lens[layout.suffix_anchor].astype(np.float64)
+    ls = layout.suffix_lens.astype(np.float64)
+    pairs = ls * la + ls * (ls + 1) / 2
+    return float(4.0 * d * hq * pairs.sum())
+
+
+def attention_bytes(layout, hq, hkv, d, kv_bytes=2) -> float:
+    """Algorithmic bytes: Q + out + lse + suffix K/V once + anchor K/V once + offsets."""
+    ts, ta = layout.total_suffix_tokens, layout.total_anchor_tokens
+    return float(ts * hq * d * 2 * 2 + ts * hq * 4 + ts * hkv * d * 2 * 2
+                 + ta * hkv * d * kv_bytes * 2
+                 + 4 * (2 * (layout.num_anchors + 1) + layout.num_suffixes + 1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_from_profile(kernel_file: str, profile_md: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
+    kernel source (the summary records the source's sha256)."""
+    path = os.path.join(ROOT, "profiles", profile_md)
+    src = os.path.join(ROOT, "prefill_only_cascade_gb300", "csrc", kernel_file)
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != sha:
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float) -> float:
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------- oracle timing
+
+def cpu_oracle_sample(layout, cfg, t_host_fn, budget_s=15.0, max_suffixes=1024):
+    """Time the float64 oracle (attention of each suffix + its head row) on host cores over a
+    seeded sample of suffixes until `budget_s` is spent. Returns tokens/s and details."""
+    import oracle
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:  # threadpoolctl is not installed everywhere
+        threads = len(os.sched_getaffinity(0))
+    ids = workloads.sample_suffixes(layout, max_suffixes, cfg.seed + 100)
+    cases = t_host_fn(ids)
+    hx = workloads.make_head_inputs(workloads.HEAD_CONFIGS["join_last_token"], "cpu",
+                                    num_rows=len(ids))
+    h64 = hx["h"].to(torch.float64).numpy()
+    g64, w64 = hx["gamma"].to(torch.float64).numpy(), hx["w8"].to(torch.float64).numpy()
+    scale = 1.0 / np.sqrt(cfg.head_dim)
+    tokens, n = 0, 0
+    t0 = time.perf_counter()
+    for j, s in enumerate(ids):
+        c = cases[int(s)]
+        oracle.suffix_attention(c["q_suf"], c["k_anc"], c["v_anc"], c["k_suf"], c["v_suf"], scale)
+        oracle.restricted_head(h64[j:j + 1], g64, w64, 1e-6)
+        tokens += c["rows"][1] - c["rows"][0]
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return tokens / dt, threads, f"{n} seeded suffixes ({tokens} tokens) of the {cfg.name} workload", dt
+
+
+def run_reference(args):
+    """--impl reference: the float64 CPU oracle, as it stands, on the host cores."""
+    world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    if rank != 0:
+        return
+    cfg = workloads.ATTN_CONFIGS[args.workload]
+    layout = workloads.make_layout(cfg)
+    # a bounded per-step sample: the same seeded suffixes every step, generated on the host
+    ids = workloads.sample_suffixes(layout, 48, cfg.seed + 200)
+    sub_anchor = sorted(set(int(layout.suffix_anchor[s]) for s in ids))
+    lens_a = [int(layout.anchor_lens[a]) for a in sub_anchor]
+    groups = [[s for s in ids if layout.suffix_anchor[s] == a] for a in sub_anchor]
+    sub = workloads.layout_from_lengths(lens_a, [len(g) for g in groups],
+                                        [int(layout.suffix_lens[s]) for g in groups for s in g])
+    t = workloads.make_attention_inputs(cfg, sub, "cpu")
+    import oracle
+    f64 = lambda x: x.to(torch.float64).numpy()
+    arr = {k: f64(t[k]) for k in ("q_suf", "k_anc", "v_anc", "k_suf", "v_suf")}
+    hx = workloads.make_head_inputs(workloads.HEAD_CONFIGS["join_last_token"], "cpu",
+                                    num_rows=sub.num_suffixes)
+    hh = [f64(hx[k]) for k in ("h", "gamma", "w8")]
+
+    def step():
+        oracle.cascade_attention(arr["q_suf"], arr["k_anc"], arr["v_anc"], arr["k_suf"],
+                                 arr["v_suf"], sub.anchor_offsets, sub.anchor_suffix_ptr,
+                                 sub.suffix_offsets)
+        oracle.restricted_head(hh[0], hh[1], hh[2], 1e-6)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = sub.total_suffix_tokens / dt
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "suffix tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{cfg.name} (bounded sample)", "sample_suffixes": int(sub.num_suffixes),
+                   "sample_tokens": int(sub.total_suffix_tokens)},
+        "cpu_baseline": {"value": value, "unit": "suffix tokens/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"{sub.num_suffixes} seeded suffixes ({sub.total_suffix_tokens} tokens) "
+                                   f"of the {cfg.name} workload with their anchors, every step"},
+        "e2e": {"value": value, "unit": "suffix tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import prefill_only_cascade_gb300 as q
+
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = workloads.ATTN_CONFIGS[args.workload]
+    layout = workloads.make_layout(cfg)
+    hq, hkv, d = cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim
+    t = workloads.make_attention_inputs(cfg, layout, dev)
+    kv_fp8 = cfg.kv_fp8
+    k_scale = v_scale = None
+    if kv_fp8:
+        ka = torch.empty(t["k_anc"].shape, dtype=torch.uint8, device=dev)
+        va = torch.empty_like(ka)
+        k_scale = torch.empty(cfg.num_anchors, hkv, dtype=torch.float32, device=dev)
+        v_scale = torch.empty_like(k_scale)
+        q.quantize_kv_fp8(t["k_anc"], t["anchor_offsets"], ka, k_scale)
+        q.quantize_kv_fp8(t["v_anc"], t["anchor_offsets"], va, v_scale)
+        t["k_anc"], t["v_anc"] = ka, va
+    desc = q.make_desc(layout.num_anchors, layout.num_suffixes, layout.total_anchor_tokens,
+                       layout.total_suffix_tokens, layout.max_anchor_len, layout.max_suffix_len,
+                       hq, hkv, d, 0.0, kv_fp8)
+    ws = torch.empty(q.cascade_workspace_size(desc), dtype=torch.uint8, device=dev)
+    out = torch.empty(layout.total_suffix_tokens, hq, d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(layout.total_suffix_tokens, hq, dtype=torch.float32, device=dev)
+    # restricted head on the last token of every suffix; hidden states of all suffix tokens
+    hcfg = workloads.HEAD_CONFIGS["join_last_token"]
+    hx = workloads.make_head_inputs(hcfg, dev, num_rows=layout.total_suffix_tokens)
+    last = torch.from_numpy((layout.suffix_offsets[1:] - 1).astype(np.int32)).to(dev)
+    S = layout.num_suffixes
+    logits = torch.empty(S, 8, dtype=torch.float32, device=dev)
+    am = torch.empty(S, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        q.cascade_attn(desc, t["q_suf"], t["k_anc"], t["v_anc"], t["k_suf"], t["v_suf"],
+                       t["anchor_offsets"], t["anchor_suffix_ptr"], t["suffix_offsets"], out,
+                       lse, ws, k_scale, v_scale, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        q.restricted_head(hx["h"], hx["gamma"], hx["w8"], logits, am, eps=hcfg.eps,
+                          row_index=last, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if q.get_device_error() != q.QUAIL_OK:
+        raise RuntimeError("device error during warm-up")
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)  # let the sampler start
+        e_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        e_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    elapsed_ms = max_over_ranks(world, e_start.elapsed_time(e_end))
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    if q.get_device_error() != q.QUAIL_OK:
+        raise RuntimeError("device error during the timed region")
+    ms_per_step = elapsed_ms / args.steps
+    tokens = layout.total_suffix_tokens * world
+    value = tokens / (ms_per_step / 1e3)
+
+    pk, src = peaks()
+    flops = attention_flops(layout, hq, d)
+    achieved_tflops = flops / (attn_ms / 1e3) / 1e12
+    peak = pk["bf16_tflops"]
+    traffic = traffic_from_profile("cascade.cu", f"cascade_attn_{cfg.name}.md")
+    roofline = {"bound": "tensor", "achieved": round(achieved_tflops, 2), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved_tflops / peak, 4),
+                "traffic": traffic, "peak_source": f"bf16_tflops (burst) of {src}",
+                "kernel": "cascade_attn_kernel (+ its schedule kernel)",
+                "kernel_ms": round(attn_ms, 4),
+                "algorithmic_flops_per_launch": flops,
+                "algorithmic_bytes_per_launch": attention_bytes(
+                    layout, hq, hkv, d, 1 if kv_fp8 else 2),
+                "hbm_frac_of_algorithmic_bytes": round(
+                    attention_bytes(layout, hq, hkv, d, 1 if kv_fp8 else 2) /
+                    (attn_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, q, desc, layout, t, hx, last, k_scale, v_scale, dev, stream, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        def host_cases(ids):
+            return workloads.gather_suffix_case(t, layout, ids)
+        if not kv_fp8:
+            v, cores, sample, dt = cpu_oracle_sample(layout, cfg, host_cases)
+            cpu = {"value": v, "unit": "suffix tokens/s", "cores": cores, "kind": "oracle",
+                   "sample": sample, "seconds": round(dt, 2)}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "suffix tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 (fp32 accumulate)" if not kv_fp8 else "bf16 Q / e4m3 anchor KV",
+        "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": cfg.name, "anchors": cfg.num_anchors,
+                   "anchor_len": list(cfg.anchor_len), "suffixes_per_anchor": cfg.suffixes_per_anchor,
+                   "suffix_len": list(cfg.suffix_len), "q_heads": hq, "kv_heads": hkv,
+                   "head_dim": d, "suffix_tokens": layout.total_suffix_tokens,
+                   "head_hidden": hcfg.hidden, "head_rows": S,
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": 3 * args.steps, "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def run_e2e(args, q, desc, layout, t, hx, last, k_scale, v_scale, dev, stream, world):
+    """Same metric through the C ABI with host buffers: every step copies its inputs from
+    pinned host memory and reads the step's result (logits and argmax) back."""
+    names = ["q_suf", "k_anc", "v_anc", "k_suf", "v_suf", "anchor_offsets",
+             "anchor_suffix_ptr", "suffix_offsets"]
+    host = {k: t[k].cpu().pin_memory() for k in names}
+    h_last = hx["h"].index_select(0, last.long()).cpu().pin_memory()
+    dev_in = {k: torch.empty_like(t[k]) for k in names}
+    h_dev = torch.empty(h_last.shape, dtype=h_last.dtype, device=dev)
+    S = layout.num_suffixes
+    logits = torch.empty(S, 8, dtype=torch.float32, device=dev)
+    am = torch.empty(S, dtype=torch.int32, device=dev)
+    logits_h = torch.empty(S, 8, dtype=torch.float32).pin_memory()
+    am_h = torch.empty(S, dtype=torch.int32).pin_memory()
+    out = torch.empty(layout.total_suffix_tokens, desc.num_q_heads, desc.head_dim,
+                      dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(q.cascade_workspace_size(desc), dtype=torch.uint8, device=dev)
+    h2d = sum(v.numel() * v.element_size() for v in host.values()) + h_last.numel() * 2
+    d2h = logits_h.numel() * 4 + am_h.numel() * 4
+
+    def step():
+        for k in names:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        h_dev.copy_(h_last, non_blocking=True)
+        q.cascade_attn(desc, dev_in["q_suf"], dev_in["k_anc"], dev_in["v_anc"], dev_in["k_suf"],
+                       dev_in["v_suf"], dev_in["anchor_offsets"], dev_in["anchor_suffix_ptr"],
+                       dev_in["suffix_offsets"], out, None, ws, k_scale, v_scale, stream=stream)
+        q.restricted_head(h_dev, hx["gamma"], hx["w8"], logits, am, eps=1e-6, stream=stream)
+        logits_h.copy_(logits, non_blocking=True)
+        am_h.copy_(am, non_blocking=True)
+
+    steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(world, a.elapsed_time(b)) / steps
+    del dev_in, h_dev, out
+    torch.cuda.empty_cache()
+    return {"value": layout.total_suffix_tokens * world / (ms / 1e3), "unit": "suffix tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": ms, "steps": steps}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

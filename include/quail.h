@@ -1,0 +1,171 @@
+/*
+ * quail.h - C ABI of libquail, the GB300 (sm_103a) hot path of Quail's prefill-only
+ * AI_JOIN / AI.IF forward step: simplified cascade attention and the 8-column restricted
+ * head.
+ *
+ * Sources (page titles and sections; the pages print no equations):
+ *   [P1] "Motor de inferência Quail atinge 1 bilhão de tokens por minuto por GPU",
+ *        section "Como funciona": zero-decode bullet and simplified-cascade-attention
+ *        bullet.
+ *   [P2] "Quail: یک میلیارد توکن در دقیقه روی یک GPU": the AI.IF join example and the
+ *        key-points list (qwen3-4b-fp8 on one GPU; head limited to 8 output tokens).
+ *
+ * Conventions for every call:
+ *   - Every pointer is DEVICE memory owned by the caller; the library never allocates or
+ *     frees memory in these calls and keeps no pointer after a call returns.
+ *   - Work is enqueued asynchronously on `stream` (NULL = the legacy default stream).
+ *   - Argument errors are found on the host and returned synchronously; nothing is
+ *     launched then. They cover NULL pointers, head counts, head_dim, dtypes and scales,
+ *     16-byte alignment, and element counts that overflow 64-bit offsets.
+ *   - Offset arrays are read on the device. A scheduling kernel checks that they are
+ *     monotone and agree with the totals and maxima of the descriptor; if not, no
+ *     attention work runs and quail_get_device_error() reports QUAIL_ERR_DEVICE_BOUNDS.
+ *   - Every wait inside a kernel is bounded; a wait that runs out sets a device error
+ *     word (QUAIL_ERR_TIMEOUT) and the kernel returns cleanly.
+ *   - No C++ exception or device trap crosses this boundary.
+ *   - The library runs on compute capability 10.3 (GB300) only; elsewhere calls return
+ *     QUAIL_ERR_UNSUPPORTED.
+ */
+#ifndef QUAIL_H_
+#define QUAIL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st* quail_stream_t;
+
+typedef enum {
+  QUAIL_OK = 0,
+  QUAIL_ERR_INVALID_ARG = 1,   /* bad argument, found on the host */
+  QUAIL_ERR_UNSUPPORTED = 2,   /* valid but not supported (head_dim, GQA ratio, device) */
+  QUAIL_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+  QUAIL_ERR_TIMEOUT = 4,       /* a bounded device-side wait ran out */
+  QUAIL_ERR_DEVICE_BOUNDS = 5  /* offsets on the device disagree with the descriptor */
+} quail_status;
+
+typedef enum { QUAIL_BF16 = 0, QUAIL_FP8_E4M3 = 1 } quail_dtype;
+
+/*
+ * Shape of one ragged cascade-attention batch. A = anchors, S = suffixes, T_A / T_S =
+ * total anchor / suffix tokens; query head h reads KV head h / (Hq / Hkv).
+ */
+typedef struct {
+  int32_t num_anchors;           /* A >= 0 */
+  int32_t num_suffixes;          /* S >= 0 */
+  int64_t total_anchor_tokens;   /* T_A = anchor_offsets[A], known on the host (no sync) */
+  int64_t total_suffix_tokens;   /* T_S = suffix_offsets[S] */
+  int32_t max_anchor_len;        /* >= every anchor length */
+  int32_t max_suffix_len;        /* >= every suffix length */
+  int32_t num_q_heads;           /* Hq, a multiple of Hkv */
+  int32_t num_kv_heads;          /* Hkv */
+  int32_t head_dim;              /* d: 64 or 128 */
+  float softmax_scale;           /* 0 => 1/sqrt(d) */
+  int32_t kv_anchor_dtype;       /* quail_dtype of k_anc/v_anc; FP8_E4M3 needs d = 128 */
+} quail_cascade_desc;
+
+/*
+ * Simplified cascade attention ([P1] "Como funciona", cascade-attention bullet): every
+ * token of a suffix attends non-causally to all tokens of its anchor (cross-attention)
+ * and causally to its own suffix's tokens up to itself; the two softmax partials are
+ * combined by LSE rescaling. The result equals softmax attention over the concatenated
+ * prompt [anchor ; suffix] of [P2]'s AI.IF example, restricted to the suffix rows.
+ *
+ *   q_suf   [T_S, Hq, d]   bf16, post-RoPE suffix queries
+ *   k_anc, v_anc [T_A, Hkv, d]  bf16, or e4m3 codes when kv_anchor_dtype = FP8_E4M3
+ *   k_suf, v_suf [T_S, Hkv, d]  bf16
+ *   anchor_offsets    [A+1] int32 token prefix sums into k_anc/v_anc
+ *   anchor_suffix_ptr [A+1] int32: the suffixes of anchor a are
+ *                     anchor_suffix_ptr[a] .. anchor_suffix_ptr[a+1]-1 (contiguous)
+ *   suffix_offsets    [S+1] int32 token prefix sums into q_suf/k_suf/v_suf/out/lse
+ *   k_scale, v_scale  [A, Hkv] fp32 dequantisation scales (value = e4m3(code) * scale);
+ *                     required for FP8_E4M3, must be NULL for BF16
+ *   out     [T_S, Hq, d] bf16 (round to nearest even from fp32)
+ *   lse     [T_S, Hq] fp32 natural log of the sum of exp(scaled scores); may be NULL
+ *   workspace: device scratch of at least quail_cascade_workspace_size(desc) bytes,
+ *              16-byte aligned; its contents are overwritten. Calls that share one
+ *              workspace must not overlap on the GPU.
+ * Empty inputs are legal (S = 0, anchors without suffixes, L_a = 0 where lse of the
+ * anchor part is -inf). Supported: d in {64, 128}, Hq/Hkv in {1, 2, 4, 8, 16}.
+ */
+quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_suf,
+                                const void* k_anc, const void* v_anc, const void* k_suf,
+                                const void* v_suf, const int32_t* anchor_offsets,
+                                const int32_t* anchor_suffix_ptr,
+                                const int32_t* suffix_offsets, const float* k_scale,
+                                const float* v_scale, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes,
+                                quail_stream_t stream);
+
+/* Workspace bytes that quail_cascade_attn needs for `desc` (0 when desc is NULL). */
+size_t quail_cascade_workspace_size(const quail_cascade_desc* desc);
+
+/*
+ * Restricted head of the zero-decode step ([P1] "Como funciona": the final prefill pass
+ * emits one token and the output vocabulary is cut to 8 options, shrinking the final
+ * unembedding matrix; [P2] key points: the head is limited to 8 output tokens). For
+ * each output row n with source row r = row_index ? row_index[n] : n:
+ *   y = h[r] * rsqrt(mean(h[r]^2) + eps) * gamma          (RMSNorm, fp32 accumulation)
+ *   logits[n, j] = sum_k y_k * w8[j, k], j < 8;  argmax[n] = lowest j with the max logit
+ *
+ *   h        bf16 rows of `hidden` elements, row r at h + r * h_row_stride elements;
+ *            h_row_stride >= hidden, (h_row_stride * 2) % 16 == 0
+ *   row_index int32 [n_rows] source rows (e.g. the last token of each suffix), or NULL
+ *   gamma    bf16 [hidden]; w8 bf16 [8, hidden] row-major
+ *   logits   fp32 [n_rows, 8]; argmax int32 [n_rows]
+ * hidden must be a positive multiple of 32 and at most 6144. n_rows may be 0.
+ */
+quail_status quail_restricted_head(int64_t n_rows, int32_t hidden, float eps, const void* h,
+                                   int64_t h_row_stride, const int32_t* row_index,
+                                   const void* gamma, const void* w8, float* logits,
+                                   int32_t* argmax, quail_stream_t stream);
+
+/*
+ * Per-(anchor, KV head) E4M3 quantisation of anchor K or V (the FP8 KV of the
+ * qwen3-4b-fp8 model named in [P2]'s key points). For anchor a and KV head g:
+ *   scale[a, g] = amax / 448 in fp32 (1 when amax == 0), amax over the anchor's tokens
+ *   and all d; code = e4m3(x / scale), x / scale rounded to fp32 first, then rounded to
+ *   nearest even with saturation at +-448 (sign kept).
+ *   kv_bf16 [T_A, Hkv, d] bf16 in; kv_e4m3 [T_A, Hkv, d] codes out; scale [A, Hkv] fp32
+ *   out. d in {64, 128}. A memset and three small kernels on `stream`.
+ */
+quail_status quail_quantize_kv_fp8(int32_t num_anchors, const int32_t* anchor_offsets,
+                                   int64_t total_anchor_tokens, int32_t num_kv_heads,
+                                   int32_t head_dim, const void* kv_bf16, void* kv_e4m3,
+                                   float* scale, quail_stream_t stream);
+
+/* Static, NUL-terminated name of a status code. */
+const char* quail_status_string(quail_status status);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device error word for the
+ * current device: QUAIL_OK, QUAIL_ERR_TIMEOUT or QUAIL_ERR_DEVICE_BOUNDS (or
+ * QUAIL_ERR_CUDA if the synchronisation itself failed).
+ */
+quail_status quail_get_device_error(quail_stream_t stream);
+
+/*
+ * Limit of every bounded device-side wait, in nanoseconds of GPU global time (default
+ * 2e9). Applies to launches made after the call. 0 restores the default.
+ */
+void quail_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Host-side fault injection for the timeout tests: with `skip_first_kv_load` != 0 the
+ * next cascade launches never issue the load of their first KV tile, so the consumer's
+ * bounded wait runs out and the launch reports QUAIL_ERR_TIMEOUT. Nothing faults.
+ */
+void quail_debug_inject(int32_t skip_first_kv_load);
+
+/* Library version, e.g. "quail-gb300 0.1". */
+const char* quail_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QUAIL_H_ */

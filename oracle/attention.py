@@ -27,6 +27,11 @@ def _expand_kv(kv: np.ndarray, num_q_heads: int) -> np.ndarray:
     return kv[:, np.arange(num_q_heads) // group, :]
 
 
+def _scores(q: np.ndarray, k: np.ndarray) -> np.ndarray:
+    """q [l, H, d], k [n, H, d] -> z [H, l, n] with z[h, i, j] = <q[i, h], k[j, h]>."""
+    return np.matmul(q.transpose(1, 0, 2), k.transpose(1, 2, 0))
+
+
 def _softmax_attend(z: np.ndarray, v: np.ndarray):
     """z [H, l, n] scores with -inf for hidden keys, v [n, H, d] -> out [l, H, d], lse [l, H].
 
@@ -40,7 +45,7 @@ def _softmax_attend(z: np.ndarray, v: np.ndarray):
     with np.errstate(divide="ignore"):
         lse = (np.log(s) + m_safe)[..., 0]
         w = np.where(s > 0, e / np.where(s > 0, s, 1.0), 0.0)
-    out = np.einsum("hij,jhd->ihd", w, v)
+    out = np.matmul(w, v.transpose(1, 0, 2)).transpose(1, 0, 2)  # sum_j w[h,i,j] v[j,h,:]
     return out, lse.T
 
 
@@ -55,7 +60,7 @@ def suffix_attention(q, k_anc, v_anc, k_suf, v_suf, scale):
     la = k_anc.shape[0]
     k = _expand_kv(np.concatenate([np.asarray(k_anc, np.float64), np.asarray(k_suf, np.float64)]), hq)
     v = _expand_kv(np.concatenate([np.asarray(v_anc, np.float64), np.asarray(v_suf, np.float64)]), hq)
-    z = scale * np.einsum("ihd,jhd->hij", q, k)
+    z = scale * _scores(q, k)
     visible = np.zeros((l, la + l), dtype=bool)
     visible[:, :la] = True
     visible[:, la:] = np.tril(np.ones((l, l), dtype=bool))
@@ -70,7 +75,7 @@ def anchor_partial(q, k_anc, v_anc, scale):
     hq = q.shape[1]
     k = _expand_kv(np.asarray(k_anc, np.float64), hq)
     v = _expand_kv(np.asarray(v_anc, np.float64), hq)
-    z = scale * np.einsum("ihd,jhd->hij", q, k)
+    z = scale * _scores(q, k)
     return _softmax_attend(z, v)
 
 
@@ -80,7 +85,7 @@ def suffix_partial(q, k_suf, v_suf, scale):
     l, hq, _ = q.shape
     k = _expand_kv(np.asarray(k_suf, np.float64), hq)
     v = _expand_kv(np.asarray(v_suf, np.float64), hq)
-    z = scale * np.einsum("ihd,jhd->hij", q, k)
+    z = scale * _scores(q, k)
     z = np.where(np.tril(np.ones((l, l), dtype=bool))[None], z, -np.inf)
     return _softmax_attend(z, v)
 

@@ -1,0 +1,177 @@
+"""Python binding of libquail: the GB300 (sm_103a) prefill-only cascade attention and
+restricted head of Quail's AI.IF / AI_JOIN step.
+
+This module only marshals arguments (tensor pointers, sizes, the current CUDA stream) to
+the C ABI declared in include/quail.h; every step of the computation runs in the
+library's CUDA kernels. PyTorch supplies device memory and streams. There is no CPU or
+PyTorch fallback: importing fails loudly when libquail.so has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libquail.so")
+
+QUAIL_OK = 0
+QUAIL_ERR_INVALID_ARG = 1
+QUAIL_ERR_UNSUPPORTED = 2
+QUAIL_ERR_CUDA = 3
+QUAIL_ERR_TIMEOUT = 4
+QUAIL_ERR_DEVICE_BOUNDS = 5
+QUAIL_BF16 = 0
+QUAIL_FP8_E4M3 = 1
+
+# Every symbol include/quail.h declares.
+EXPORTED_SYMBOLS = (
+    "quail_cascade_attn", "quail_cascade_workspace_size", "quail_restricted_head",
+    "quail_quantize_kv_fp8", "quail_status_string", "quail_get_device_error",
+    "quail_set_wait_timeout_ns", "quail_debug_inject", "quail_version",
+)
+
+
+class QuailError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class CascadeDesc(ctypes.Structure):
+    _fields_ = [
+        ("num_anchors", ctypes.c_int32),
+        ("num_suffixes", ctypes.c_int32),
+        ("total_anchor_tokens", ctypes.c_int64),
+        ("total_suffix_tokens", ctypes.c_int64),
+        ("max_anchor_len", ctypes.c_int32),
+        ("max_suffix_len", ctypes.c_int32),
+        ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("softmax_scale", ctypes.c_float),
+        ("kv_anchor_dtype", ctypes.c_int32),
+    ]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -m prefill_only_cascade_gb300.build` "
+            "(there is no fallback implementation)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32p, f32p = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+    lib.quail_cascade_attn.argtypes = [ctypes.POINTER(CascadeDesc), vp, vp, vp, vp, vp, i32p,
+                                       i32p, i32p, f32p, f32p, vp, f32p, vp, ctypes.c_size_t, vp]
+    lib.quail_cascade_attn.restype = ctypes.c_int
+    lib.quail_cascade_workspace_size.argtypes = [ctypes.POINTER(CascadeDesc)]
+    lib.quail_cascade_workspace_size.restype = ctypes.c_size_t
+    lib.quail_restricted_head.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_float, vp,
+                                          ctypes.c_int64, i32p, vp, vp, f32p, i32p, vp]
+    lib.quail_restricted_head.restype = ctypes.c_int
+    lib.quail_quantize_kv_fp8.argtypes = [ctypes.c_int32, i32p, ctypes.c_int64, ctypes.c_int32,
+                                          ctypes.c_int32, vp, vp, f32p, vp]
+    lib.quail_quantize_kv_fp8.restype = ctypes.c_int
+    lib.quail_status_string.argtypes = [ctypes.c_int]
+    lib.quail_status_string.restype = ctypes.c_char_p
+    lib.quail_get_device_error.argtypes = [vp]
+    lib.quail_get_device_error.restype = ctypes.c_int
+    lib.quail_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    lib.quail_set_wait_timeout_ns.restype = None
+    lib.quail_debug_inject.argtypes = [ctypes.c_int32]
+    lib.quail_debug_inject.restype = None
+    lib.quail_version.argtypes = []
+    lib.quail_version.restype = ctypes.c_char_p
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.quail_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return lib.quail_version().decode()
+
+
+def _check(status: int, what: str):
+    if status != QUAIL_OK:
+        raise QuailError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_desc(num_anchors, num_suffixes, total_anchor_tokens, total_suffix_tokens,
+              max_anchor_len, max_suffix_len, num_q_heads, num_kv_heads, head_dim,
+              softmax_scale=0.0, kv_fp8=False) -> CascadeDesc:
+    return CascadeDesc(int(num_anchors), int(num_suffixes), int(total_anchor_tokens),
+                       int(total_suffix_tokens), int(max_anchor_len), int(max_suffix_len),
+                       int(num_q_heads), int(num_kv_heads), int(head_dim), float(softmax_scale),
+                       QUAIL_FP8_E4M3 if kv_fp8 else QUAIL_BF16)
+
+
+def cascade_workspace_size(desc: CascadeDesc) -> int:
+    return int(lib.quail_cascade_workspace_size(ctypes.byref(desc)))
+
+
+def cascade_attn(desc: CascadeDesc, q_suf, k_anc, v_anc, k_suf, v_suf, anchor_offsets,
+                 anchor_suffix_ptr, suffix_offsets, out, lse=None, workspace=None,
+                 k_scale=None, v_scale=None, stream=None):
+    """quail_cascade_attn on torch CUDA tensors (see include/quail.h for layouts)."""
+    if workspace is None:
+        raise ValueError("workspace is required (size: cascade_workspace_size(desc))")
+    st = lib.quail_cascade_attn(
+        ctypes.byref(desc), _ptr(q_suf), _ptr(k_anc), _ptr(v_anc), _ptr(k_suf), _ptr(v_suf),
+        _ptr(anchor_offsets), _ptr(anchor_suffix_ptr), _ptr(suffix_offsets), _ptr(k_scale),
+        _ptr(v_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(stream))
+    _check(st, "quail_cascade_attn")
+
+
+def restricted_head(h, gamma, w8, logits, argmax, eps=1e-6, row_index=None, n_rows=None,
+                    stream=None):
+    """quail_restricted_head: RMSNorm + 8-column head + argmax over rows of h (or over
+    h[row_index])."""
+    if n_rows is None:
+        n_rows = row_index.numel() if row_index is not None else h.shape[0]
+    st = lib.quail_restricted_head(int(n_rows), int(h.shape[-1]), float(eps), _ptr(h),
+                                   int(h.stride(0)), _ptr(row_index), _ptr(gamma), _ptr(w8),
+                                   _ptr(logits), _ptr(argmax), _stream(stream))
+    _check(st, "quail_restricted_head")
+
+
+def quantize_kv_fp8(kv_bf16, anchor_offsets, codes, scale, stream=None):
+    """quail_quantize_kv_fp8: per-(anchor, KV head) E4M3 codes and fp32 scales."""
+    T, hkv, d = kv_bf16.shape
+    st = lib.quail_quantize_kv_fp8(int(anchor_offsets.numel() - 1), _ptr(anchor_offsets), int(T),
+                                   int(hkv), int(d), _ptr(kv_bf16), _ptr(codes), _ptr(scale),
+                                   _stream(stream))
+    _check(st, "quail_quantize_kv_fp8")
+
+
+def get_device_error(stream=None) -> int:
+    return int(lib.quail_get_device_error(_stream(stream)))
+
+
+def set_wait_timeout_ns(ns: int):
+    lib.quail_set_wait_timeout_ns(int(ns))
+
+
+def debug_inject(skip_first_kv_load: bool):
+    lib.quail_debug_inject(1 if skip_first_kv_load else 0)
+
+
+def default_scale(head_dim: int) -> float:
+    return 1.0 / math.sqrt(head_dim)

@@ -1,0 +1,302 @@
+// api.cu - the C ABI of libquail (declared in include/quail.h): argument validation on
+// the host, tensor-map encoding, and launches on the caller's stream. No call allocates.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "quail.h"
+
+namespace {
+
+// The library's device error word (one per device context). Kernels OR bits into it;
+// quail_get_device_error() reads and clears it.
+__device__ unsigned g_quail_error_word;
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+struct DeviceState {
+  bool ready = false;
+  quail_status status = QUAIL_ERR_CUDA;
+  int num_sms = 0;
+  unsigned* err_word = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+uint64_t g_timeout_ns = kDefaultTimeoutNs;
+int g_inject_skip = 0;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Per-device set-up: the device must be a GB300 (compute capability 10.3).
+quail_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QUAIL_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    st.ready = true;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+      st.status = QUAIL_ERR_CUDA;
+    } else if (prop.major != 10 || prop.minor != 3) {
+      st.status = QUAIL_ERR_UNSUPPORTED;
+    } else if (cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err_word),
+                                    g_quail_error_word) != cudaSuccess) {
+      st.status = QUAIL_ERR_CUDA;
+    } else {
+      st.num_sms = prop.multiProcessorCount;
+      st.status = QUAIL_OK;
+      if (g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr) {
+          st.status = QUAIL_ERR_CUDA;
+        } else {
+          g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+      }
+    }
+  }
+  *out = &st;
+  return st.status;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 3-D bf16 tensor map over [tokens, heads, d] (innermost d), 128-byte swizzle, box
+// (64 elements of d, box_heads, box_rows); out-of-range rows read as zero.
+bool encode_3d(CUtensorMap* m, const void* base, int64_t tokens, int heads, int d,
+               int box_heads, int box_rows, CUtensorMapDataType dt, int elem_bytes, int box_inner) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(tokens)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elem_bytes,
+                                 static_cast<cuuint64_t>(heads) * d * elem_bytes};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_inner),
+                             static_cast<cuuint32_t>(box_heads),
+                             static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool valid_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16; }
+
+}  // namespace
+
+extern "C" {
+
+const char* quail_version(void) { return "quail-gb300 0.1"; }
+
+const char* quail_status_string(quail_status s) {
+  switch (s) {
+    case QUAIL_OK: return "QUAIL_OK";
+    case QUAIL_ERR_INVALID_ARG: return "QUAIL_ERR_INVALID_ARG";
+    case QUAIL_ERR_UNSUPPORTED: return "QUAIL_ERR_UNSUPPORTED";
+    case QUAIL_ERR_CUDA: return "QUAIL_ERR_CUDA";
+    case QUAIL_ERR_TIMEOUT: return "QUAIL_ERR_TIMEOUT";
+    case QUAIL_ERR_DEVICE_BOUNDS: return "QUAIL_ERR_DEVICE_BOUNDS";
+  }
+  return "QUAIL_ERR_UNKNOWN";
+}
+
+void quail_set_wait_timeout_ns(uint64_t ns) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  g_timeout_ns = ns == 0 ? kDefaultTimeoutNs : ns;
+}
+
+void quail_debug_inject(int32_t skip_first_kv_load) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  g_inject_skip = skip_first_kv_load != 0;
+}
+
+size_t quail_cascade_workspace_size(const quail_cascade_desc* desc) {
+  if (desc == nullptr || desc->num_anchors < 0) return 0;
+  return quail::cascade_workspace_bytes(desc->num_anchors);
+}
+
+quail_status quail_get_device_error(quail_stream_t stream) {
+  DeviceState* st = nullptr;
+  const quail_status s = device_state(&st);
+  if (s != QUAIL_OK) return s;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return QUAIL_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, st->err_word, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return QUAIL_ERR_CUDA;
+  if (word == 0) return QUAIL_OK;
+  if (cudaMemset(st->err_word, 0, sizeof(unsigned)) != cudaSuccess) return QUAIL_ERR_CUDA;
+  if (word & quail::kErrTimeout) return QUAIL_ERR_TIMEOUT;
+  return QUAIL_ERR_DEVICE_BOUNDS;
+}
+
+quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_suf,
+                                const void* k_anc, const void* v_anc, const void* k_suf,
+                                const void* v_suf, const int32_t* anchor_offsets,
+                                const int32_t* anchor_suffix_ptr,
+                                const int32_t* suffix_offsets, const float* k_scale,
+                                const float* v_scale, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes,
+                                quail_stream_t stream) {
+  if (desc == nullptr) return QUAIL_ERR_INVALID_ARG;
+  const quail_cascade_desc& d = *desc;
+  const int64_t kMaxTok = (1ll << 31) - 1;
+  if (d.num_anchors < 0 || d.num_suffixes < 0 || d.total_anchor_tokens < 0 ||
+      d.total_suffix_tokens < 0 || d.total_anchor_tokens > kMaxTok ||
+      d.total_suffix_tokens > kMaxTok || d.max_anchor_len < 0 || d.max_suffix_len < 0)
+    return QUAIL_ERR_INVALID_ARG;
+  if (d.num_q_heads <= 0 || d.num_kv_heads <= 0 || d.num_q_heads % d.num_kv_heads != 0)
+    return QUAIL_ERR_INVALID_ARG;
+  if (!(d.softmax_scale >= 0.0f) || !std::isfinite(d.softmax_scale)) return QUAIL_ERR_INVALID_ARG;
+  if (d.kv_anchor_dtype != QUAIL_BF16 && d.kv_anchor_dtype != QUAIL_FP8_E4M3)
+    return QUAIL_ERR_INVALID_ARG;
+  const bool fp8 = d.kv_anchor_dtype == QUAIL_FP8_E4M3;
+  if (fp8 ? (k_scale == nullptr || v_scale == nullptr) : (k_scale != nullptr || v_scale != nullptr))
+    return QUAIL_ERR_INVALID_ARG;
+  if (d.num_suffixes == 0 && d.total_suffix_tokens != 0) return QUAIL_ERR_INVALID_ARG;
+  if (d.num_anchors == 0 && (d.num_suffixes != 0 || d.total_anchor_tokens != 0))
+    return QUAIL_ERR_INVALID_ARG;
+  const int group = d.num_q_heads / d.num_kv_heads;
+  if (d.head_dim != 64 && d.head_dim != 128) return QUAIL_ERR_UNSUPPORTED;
+  if (!valid_group(group)) return QUAIL_ERR_UNSUPPORTED;
+  if (fp8 && d.head_dim != 128) return QUAIL_ERR_UNSUPPORTED;
+  if (anchor_offsets == nullptr || anchor_suffix_ptr == nullptr || suffix_offsets == nullptr)
+    return QUAIL_ERR_INVALID_ARG;
+  if (d.total_suffix_tokens > 0) {
+    if (q_suf == nullptr || k_suf == nullptr || v_suf == nullptr || out == nullptr)
+      return QUAIL_ERR_INVALID_ARG;
+    if (!aligned16(q_suf) || !aligned16(k_suf) || !aligned16(v_suf) || !aligned16(out))
+      return QUAIL_ERR_INVALID_ARG;
+  }
+  if (d.total_anchor_tokens > 0) {
+    if (k_anc == nullptr || v_anc == nullptr) return QUAIL_ERR_INVALID_ARG;
+    if (!aligned16(k_anc) || !aligned16(v_anc)) return QUAIL_ERR_INVALID_ARG;
+  }
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return QUAIL_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(anchor_offsets) | reinterpret_cast<uintptr_t>(anchor_suffix_ptr) |
+       reinterpret_cast<uintptr_t>(suffix_offsets)) & 3u)
+    return QUAIL_ERR_INVALID_ARG;
+  const size_t need = quail::cascade_workspace_bytes(d.num_anchors);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+    return QUAIL_ERR_INVALID_ARG;
+  if (fp8) return QUAIL_ERR_UNSUPPORTED;  // the FP8 anchor path is not built yet
+
+  DeviceState* st = nullptr;
+  const quail_status ds = device_state(&st);
+  if (ds != QUAIL_OK) return ds;
+  if (d.total_suffix_tokens == 0) return QUAIL_OK;  // nothing to compute
+
+  const int D = d.head_dim;
+  const int tok = 128 / group;
+  quail::CascadeMaps maps;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  bool ok = encode_3d(&maps.q, q_suf, d.total_suffix_tokens, d.num_q_heads, D, group, tok, bf, 2, 64) &&
+            encode_3d(&maps.k_suf, k_suf, d.total_suffix_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64) &&
+            encode_3d(&maps.v_suf, v_suf, d.total_suffix_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64);
+  if (d.total_anchor_tokens > 0) {
+    ok = ok && encode_3d(&maps.k_anc, k_anc, d.total_anchor_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64) &&
+         encode_3d(&maps.v_anc, v_anc, d.total_anchor_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64);
+  } else {
+    maps.k_anc = maps.k_suf;  // never read: every anchor is empty
+    maps.v_anc = maps.v_suf;
+  }
+  if (!ok) return QUAIL_ERR_CUDA;
+
+  quail::CascadeParams p;
+  p.num_anchors = d.num_anchors;
+  p.num_suffixes = d.num_suffixes;
+  p.total_anchor_tokens = d.total_anchor_tokens;
+  p.total_suffix_tokens = d.total_suffix_tokens;
+  p.max_anchor_len = d.max_anchor_len;
+  p.max_suffix_len = d.max_suffix_len;
+  p.hq = d.num_q_heads;
+  p.hkv = d.num_kv_heads;
+  p.group = group;
+  p.tok_per_tile = tok;
+  const float scale = d.softmax_scale > 0.0f ? d.softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.fp8 = fp8;
+  p.anchor_offsets = anchor_offsets;
+  p.anchor_suffix_ptr = anchor_suffix_ptr;
+  p.suffix_offsets = suffix_offsets;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.k_anc = k_anc;
+  p.v_anc = v_anc;
+  p.out = out;
+  p.lse = lse;
+  p.sched = static_cast<int32_t*>(workspace);
+  p.err_word = st->err_word;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    p.timeout_ns = g_timeout_ns;
+    p.inject_skip_first_kv = g_inject_skip;
+  }
+  const cudaError_t e = quail::launch_cascade(p, maps, D, st->num_sms,
+                                              reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QUAIL_OK : QUAIL_ERR_CUDA;
+}
+
+quail_status quail_restricted_head(int64_t n_rows, int32_t hidden, float eps, const void* h,
+                                   int64_t h_row_stride, const int32_t* row_index,
+                                   const void* gamma, const void* w8, float* logits,
+                                   int32_t* argmax, quail_stream_t stream) {
+  if (n_rows < 0 || hidden <= 0 || hidden % 32 != 0 || !(eps >= 0.0f) || !std::isfinite(eps))
+    return QUAIL_ERR_INVALID_ARG;
+  if (hidden > 6144) return QUAIL_ERR_UNSUPPORTED;
+  if (h_row_stride < hidden || (h_row_stride * 2) % 16 != 0) return QUAIL_ERR_INVALID_ARG;
+  if (n_rows > 0) {
+    if (h == nullptr || gamma == nullptr || w8 == nullptr || logits == nullptr || argmax == nullptr)
+      return QUAIL_ERR_INVALID_ARG;
+    if (!aligned16(h) || !aligned16(logits) || (reinterpret_cast<uintptr_t>(argmax) & 3u) ||
+        (reinterpret_cast<uintptr_t>(gamma) & 1u) || (reinterpret_cast<uintptr_t>(w8) & 1u) ||
+        (reinterpret_cast<uintptr_t>(row_index) & 3u))
+      return QUAIL_ERR_INVALID_ARG;
+  }
+  DeviceState* st = nullptr;
+  const quail_status ds = device_state(&st);
+  if (ds != QUAIL_OK) return ds;
+  quail::HeadArgs a{n_rows, hidden, eps, h, h_row_stride, row_index, gamma, w8, logits, argmax};
+  const cudaError_t e =
+      quail::launch_restricted_head(a, st->num_sms, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QUAIL_OK : QUAIL_ERR_CUDA;
+}
+
+quail_status quail_quantize_kv_fp8(int32_t num_anchors, const int32_t* anchor_offsets,
+                                   int64_t total_anchor_tokens, int32_t num_kv_heads,
+                                   int32_t head_dim, const void* kv_bf16, void* kv_e4m3,
+                                   float* scale, quail_stream_t stream) {
+  if (num_anchors < 0 || total_anchor_tokens < 0 || total_anchor_tokens > (1ll << 31) - 1 ||
+      num_kv_heads <= 0)
+    return QUAIL_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return QUAIL_ERR_UNSUPPORTED;
+  if (num_anchors == 0 && total_anchor_tokens != 0) return QUAIL_ERR_INVALID_ARG;
+  if (num_anchors > 0 && (anchor_offsets == nullptr || scale == nullptr)) return QUAIL_ERR_INVALID_ARG;
+  if (total_anchor_tokens > 0 &&
+      (kv_bf16 == nullptr || kv_e4m3 == nullptr || !aligned16(kv_bf16) || !aligned16(kv_e4m3)))
+    return QUAIL_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(scale) | reinterpret_cast<uintptr_t>(anchor_offsets)) & 3u)
+    return QUAIL_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  const quail_status ds = device_state(&st);
+  if (ds != QUAIL_OK) return ds;
+  quail::QuantArgs q{num_anchors, anchor_offsets, total_anchor_tokens, num_kv_heads, head_dim,
+                     kv_bf16, kv_e4m3, scale};
+  const cudaError_t e =
+      quail::launch_quantize_kv_fp8(q, st->num_sms, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QUAIL_OK : QUAIL_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,70 @@
+// kernels.h - internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace quail {
+
+struct HeadArgs {
+  int64_t n_rows;
+  int hidden;
+  float eps;
+  const void* h;
+  int64_t h_row_stride;
+  const int32_t* row_index;
+  const void* gamma;
+  const void* w8;
+  float* logits;
+  int32_t* argmax;
+};
+size_t restricted_head_smem_bytes(int hidden);
+cudaError_t launch_restricted_head(const HeadArgs& a, int num_sms, cudaStream_t stream);
+
+struct QuantArgs {
+  int num_anchors;
+  const int32_t* anchor_offsets;
+  int64_t total_tokens;
+  int num_kv_heads;
+  int head_dim;
+  const void* kv;
+  void* codes;
+  float* scale;
+};
+cudaError_t launch_quantize_kv_fp8(const QuantArgs& q, int num_sms, cudaStream_t stream);
+
+// Everything the cascade kernels need besides the tensor maps.
+struct CascadeParams {
+  int num_anchors, num_suffixes;
+  int64_t total_anchor_tokens, total_suffix_tokens;
+  int max_anchor_len, max_suffix_len;
+  int hq, hkv, group;        // group = hq / hkv
+  int tok_per_tile;          // 128 / group suffix tokens per 128-row query tile
+  float scale_log2;          // softmax_scale * log2(e)
+  bool fp8;
+  const int32_t* anchor_offsets;
+  const int32_t* anchor_suffix_ptr;
+  const int32_t* suffix_offsets;
+  const float* k_scale;
+  const float* v_scale;
+  const void* k_anc;         // raw pointers (the FP8 path reads anchor codes directly)
+  const void* v_anc;
+  void* out;
+  float* lse;
+  int32_t* sched;            // workspace: [A+1] item prefix, then [A] anchor order
+  unsigned* err_word;
+  uint64_t timeout_ns;
+  int inject_skip_first_kv;
+};
+
+// Tensor maps over q_suf, k/v anchor and k/v suffix (bf16, 3-D: d, head, token).
+struct CascadeMaps {
+  CUtensorMap q, k_anc, v_anc, k_suf, v_suf;
+};
+
+size_t cascade_workspace_bytes(int num_anchors);
+cudaError_t launch_cascade(const CascadeParams& p, const CascadeMaps& maps, int head_dim,
+                           int num_sms, cudaStream_t stream);
+
+}  // namespace quail

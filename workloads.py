@@ -206,18 +206,19 @@ def gather_suffix_case(tensors: dict, layout: RaggedLayout, suffix_ids) -> dict:
     workload to the CPU oracle."""
     so = layout.suffix_offsets.astype(np.int64)
     ao = layout.anchor_offsets.astype(np.int64)
-    out = {}
+    out, anchors = {}, {}
     for s in suffix_ids:
         s = int(s)
         a = int(layout.suffix_anchor[s])
         r0, r1 = int(so[s]), int(so[s + 1])
-        a0, a1 = int(ao[a]), int(ao[a + 1])
         case = {"anchor": a, "rows": (r0, r1)}
         for key in ("q_suf", "k_suf", "v_suf"):
             case[key] = _to_np(tensors[key][r0:r1])
-        for key in ("k_anc", "v_anc"):
-            if key in tensors:
-                case[key] = _to_np(tensors[key][a0:a1])
+        if a not in anchors:  # one host copy per anchor, shared by its suffixes
+            a0, a1 = int(ao[a]), int(ao[a + 1])
+            anchors[a] = {key: _to_np(tensors[key][a0:a1]) for key in ("k_anc", "v_anc")
+                          if tensors.get(key) is not None}
+        case.update(anchors[a])
         out[s] = case
     return out
 
