@@ -59,7 +59,7 @@ class CascadeDesc(ctypes.Structure):
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
-            f"{LIB_PATH} is missing: build it with `python -m prefill_only_cascade_gb300.build` "
+            f"{LIB_PATH} is missing: build it with `python prefill_only_cascade_gb300/build.py` "
             "(there is no fallback implementation)")
     lib = ctypes.CDLL(LIB_PATH)
     vp, i32p, f32p = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p

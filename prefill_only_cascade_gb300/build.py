@@ -2,7 +2,7 @@
 
 Each translation unit in csrc/ is compiled in parallel to an object under _build/, then
 linked into prefill_only_cascade_gb300/libquail.so (CUDA runtime linked statically).
-Run: python -m prefill_only_cascade_gb300.build
+Run: python prefill_only_cascade_gb300/build.py
 """
 from __future__ import annotations
 
