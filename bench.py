@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--workload", default="join", choices=["join", "ragged", "fp8_long"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--suffixes-per-anchor", type=int, default=None,
+                    help="smaller case of the same workload (profiling only)")
     return ap.parse_args()
 
 
@@ -256,12 +258,16 @@ def run_reference(args):
 # ---------------------------------------------------------------------------- our arm
 
 def run_ours(args):
+    import dataclasses
+
     import prefill_only_cascade_gb300 as q
 
     world, rank, local = dist_setup(args.gpus)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     cfg = workloads.ATTN_CONFIGS[args.workload]
+    if args.suffixes_per_anchor:
+        cfg = dataclasses.replace(cfg, suffixes_per_anchor=args.suffixes_per_anchor)
     layout = workloads.make_layout(cfg)
     hq, hkv, d = cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim
     t = workloads.make_attention_inputs(cfg, layout, dev)
