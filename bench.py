@@ -377,7 +377,7 @@ def run_ours(args):
                    "head_hidden": hcfg.hidden, "head_rows": S,
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": 3 * args.steps, "clocks": clk.summary(),
+        "gpu_launches": 5 * args.steps, "clocks": clk.summary(),
     }
     if rank == 0:
         print(json.dumps(line))

@@ -123,8 +123,15 @@ void quail_debug_inject(int32_t skip_first_kv_load) {
 }
 
 size_t quail_cascade_workspace_size(const quail_cascade_desc* desc) {
-  if (desc == nullptr || desc->num_anchors < 0) return 0;
-  return quail::cascade_workspace_bytes(desc->num_anchors);
+  if (desc == nullptr || desc->num_anchors < 0 || desc->total_suffix_tokens < 0 ||
+      desc->num_q_heads <= 0 || desc->num_kv_heads <= 0 ||
+      desc->num_q_heads % desc->num_kv_heads != 0 ||
+      !valid_group(desc->num_q_heads / desc->num_kv_heads))
+    return 0;
+  const int64_t bound = quail::cascade_item_bound(
+      desc->num_anchors, desc->total_suffix_tokens, desc->num_kv_heads,
+      desc->num_q_heads / desc->num_kv_heads);
+  return quail::cascade_workspace_layout(desc->num_anchors, desc->total_suffix_tokens, bound).total;
 }
 
 quail_status quail_get_device_error(quail_stream_t stream) {
@@ -188,8 +195,12 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
   if ((reinterpret_cast<uintptr_t>(anchor_offsets) | reinterpret_cast<uintptr_t>(anchor_suffix_ptr) |
        reinterpret_cast<uintptr_t>(suffix_offsets)) & 3u)
     return QUAIL_ERR_INVALID_ARG;
-  const size_t need = quail::cascade_workspace_bytes(d.num_anchors);
-  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+  const int64_t item_bound =
+      quail::cascade_item_bound(d.num_anchors, d.total_suffix_tokens, d.num_kv_heads, group);
+  if (item_bound > (1ll << 31) - 1) return QUAIL_ERR_UNSUPPORTED;
+  const quail::CascadeWorkspace wl =
+      quail::cascade_workspace_layout(d.num_anchors, d.total_suffix_tokens, item_bound);
+  if (workspace == nullptr || workspace_bytes < wl.total || !aligned16(workspace))
     return QUAIL_ERR_INVALID_ARG;
   if (fp8) return QUAIL_ERR_UNSUPPORTED;  // the FP8 anchor path is not built yet
 
@@ -237,7 +248,13 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
   p.v_anc = v_anc;
   p.out = out;
   p.lse = lse;
-  p.sched = static_cast<int32_t*>(workspace);
+  p.item_bound = static_cast<int>(item_bound);
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  p.flag = reinterpret_cast<int32_t*>(wsb + wl.flag);
+  p.prefix = reinterpret_cast<int32_t*>(wsb + wl.prefix);
+  p.order = reinterpret_cast<int32_t*>(wsb + wl.order);
+  p.seg = reinterpret_cast<int32_t*>(wsb + wl.seg);
+  p.items = reinterpret_cast<int32_t*>(wsb + wl.items);
   p.err_word = st->err_word;
   {
     std::lock_guard<std::mutex> lock(g_mutex);

@@ -15,15 +15,27 @@
 // anchor keys with no mask, so any tokens of the anchor's suffixes can share a tile; the
 // suffix part uses a per-row key window [start of the row's suffix, the row's token].
 //
-// Per CTA (one per SM, persistent):
+// Launch sequence on the caller's stream (all scratch lives in the caller's workspace):
+//   1. memset of the check flag
+//   2. cascade_segments_kernel  (grid)   per-suffix offset checks; seg[t] = start of the
+//                                        suffix holding token t
+//   3. cascade_schedule_kernel  (1 CTA)  anchor checks; anchors ordered by decreasing
+//                                        anchor-tile count; prefix sum of work items
+//   4. cascade_items_kernel     (grid)   one 32-byte record per work item
+//   5. cascade_attn_kernel      (persistent, one CTA per SM)
+//
+// Per CTA of the attention kernel:
 //   warp 8      TMA producer: Q tiles, then a ring of K / V tiles (128 keys each)
 //   warp 9      MMA issuer:   S_q = Q_q K^T (SMEM x SMEM -> TMEM), O_q += P_q V
 //                             (P from TMEM, V from SMEM), tcgen05 kind::f16, M = 128
 //   warps 0-3   softmax of query tile 0, one thread per TMEM lane (= query row)
 //   warps 4-7   softmax of query tile 1
+//   warps 10-11 idle (they complete the third warpgroup for the register split)
 // TMEM (512 columns): tile q uses S/P at columns 256q .. +127 and O at 256q+128 .. +255.
 // The two query tiles share every anchor KV tile loaded into shared memory and ping-pong:
 // while one warpgroup exponentiates its scores the tensor core works on the other tile.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -35,7 +47,13 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;             // three warpgroups
+// Register split (setmaxnreg): the two softmax warpgroups grow to kRegsSoftmax, the
+// producer/MMA warpgroup shrinks to kRegsOther. 256 * 184 + 128 * 136 = 64,512 registers,
+// which must not exceed the 384 * (registers at launch) the block holds; the host checks
+// the compiled register count before launching.
+constexpr int kRegsSoftmax = 184;
+constexpr int kRegsOther = 136;
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: O is rescaled only past 2^8
@@ -62,75 +80,43 @@ struct __align__(8) Bars {
   int abort_flag;
 };
 
+// One work item as written by cascade_items_kernel (two int4).
 struct Item {
-  int a, g;
-  int a_tok0, la;      // anchor token start (into k_anc/v_anc) and length
-  int s_lo, s_hi;      // suffix index range of the anchor
-  int t0;              // first suffix token of query tile 0
-  int n_anchor_tiles;  // ceil(la / 128)
-  int n_sfx_tiles;     // suffix-window tiles per query tile
-  int nk_sfx;          // keys per suffix tile (64 or 128)
-  int ws0, ws1;        // suffix window start of query tile 0 / 1
-  int tend0, tend1;    // one past the last valid token of query tile 0 / 1
+  int a_tok0, la;   // anchor token start (into k_anc/v_anc) and length
+  int t0, g;        // first suffix token of query tile 0; KV head
+  int ws0, ws1;     // suffix key window start of query tile 0 / 1
+  int tend0, tend1; // one past the last valid token of query tile 0 / 1 (tend == start: empty)
   __device__ __forceinline__ int ws(int q) const { return q ? ws1 : ws0; }
   __device__ __forceinline__ int tend(int q) const { return q ? tend1 : tend0; }
+  __device__ __forceinline__ int n_anchor_tiles() const { return (la + kBN - 1) / kBN; }
+  __device__ __forceinline__ int window() const { return max(tend0 - ws0, tend1 - ws1); }
+  __device__ __forceinline__ int n_sfx_tiles() const { return (window() + kBN - 1) / kBN; }
+  __device__ __forceinline__ int nk_sfx() const {
+    return (n_sfx_tiles() == 1 && window() <= 64) ? 64 : 128;
+  }
 };
 
-// Start token of the suffix (of the anchor's range [s_lo, s_hi)) that contains token t.
-__device__ __forceinline__ int seg_start(const int32_t* __restrict__ so, int s_lo, int s_hi,
-                                         int t) {
-  int lo = s_lo, hi = s_hi - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(so + mid) <= t) lo = mid; else hi = mid - 1;
-  }
-  return __ldg(so + lo);
+__device__ __forceinline__ int4 ld_nc_v4(const int32_t* p) {
+  int4 v;
+  asm volatile("ld.global.nc.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
 }
 
-__device__ __forceinline__ void decode_item(const CascadeParams& p, int item, Item& it) {
-  const int A = p.num_anchors;
-  const int32_t* prefix = p.sched;
-  const int32_t* order = p.sched + A + 1;
-  int lo = 0, hi = A - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(prefix + mid) <= item) lo = mid; else hi = mid - 1;
-  }
-  const int a = __ldg(order + lo);
-  const int local = item - __ldg(prefix + lo);
-  it.a = a;
-  it.s_lo = __ldg(p.anchor_suffix_ptr + a);
-  it.s_hi = __ldg(p.anchor_suffix_ptr + a + 1);
-  const int s_begin = __ldg(p.suffix_offsets + it.s_lo);
-  const int s_end = __ldg(p.suffix_offsets + it.s_hi);
-  const int tok = p.tok_per_tile;
-  const int pairs = (s_end - s_begin + 2 * tok - 1) / (2 * tok);
-  it.g = local / pairs;
-  it.t0 = s_begin + (local % pairs) * 2 * tok;
-  it.a_tok0 = __ldg(p.anchor_offsets + a);
-  it.la = __ldg(p.anchor_offsets + a + 1) - it.a_tok0;
-  it.n_anchor_tiles = (it.la + kBN - 1) / kBN;
-  // query tile 0 always holds at least one token of the anchor
-  it.tend0 = min(it.t0 + tok, s_end);
-  it.ws0 = seg_start(p.suffix_offsets, it.s_lo, it.s_hi, it.t0);
-  int wmax = it.tend0 - it.ws0;
-  const int t1 = it.t0 + tok;
-  if (s_end > t1) {
-    it.tend1 = min(t1 + tok, s_end);
-    it.ws1 = seg_start(p.suffix_offsets, it.s_lo, it.s_hi, t1);
-    wmax = max(wmax, it.tend1 - it.ws1);
-  } else {
-    it.tend1 = t1;
-    it.ws1 = t1;
-  }
-  it.n_sfx_tiles = (wmax + kBN - 1) / kBN;
-  it.nk_sfx = (it.n_sfx_tiles == 1 && wmax <= 64) ? 64 : 128;
+__device__ __forceinline__ Item load_item(const CascadeParams& p, int item) {
+  const int4 a = ld_nc_v4(p.items + 8 * static_cast<int64_t>(item));
+  const int4 b = ld_nc_v4(p.items + 8 * static_cast<int64_t>(item) + 4);
+  Item it;
+  it.a_tok0 = a.x; it.la = a.y; it.t0 = a.z; it.g = a.w;
+  it.ws0 = b.x; it.ws1 = b.y; it.tend0 = b.z; it.tend1 = b.w;
+  return it;
 }
 
 // Ring position -> what it holds: anchor tile k (k < nA) or the suffix tile i of query
 // tile q at position nA + 2i + q.
-__device__ __forceinline__ int pos_of(const Item& it, int q, int k) {
-  return k < it.n_anchor_tiles ? k : it.n_anchor_tiles + 2 * (k - it.n_anchor_tiles) + q;
+__device__ __forceinline__ int pos_of(int nA, int q, int k) {
+  return k < nA ? k : nA + 2 * (k - nA) + q;
 }
 
 __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity, uint64_t deadline) {
@@ -146,6 +132,35 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// Packed pairs of fp32 (one 64-bit register pair, f32x2 arithmetic).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -153,33 +168,40 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // ---------------------------------------------------------------------------------
-// Softmax of one S tile held in registers: mask, row max, lazy rescale of O, P = 2^(s c - m)
+// Softmax of one S tile of NC columns: mask, row max, lazy rescale of O, P = 2^(s c - m)
 // written back to TMEM as bf16 (columns 0 .. NC/2 of the S region), row sum update.
 template <int NC, int D>
 __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, bool first_tile,
                                              bool masked, int lo_c, int hi_c, float c,
                                              float& m_used, float& l) {
+  uint32_t r[NC / 32][32];
+#pragma unroll
+  for (int ch = 0; ch < NC / 32; ++ch) tmem_ld32(t_s + ch * 32, r[ch]);
+  tmem_wait_ld_dep(r[0]);
+#pragma unroll
+  for (int ch = 1; ch < NC / 32; ++ch) reg_dep(r[ch]);
   float s[NC];
-  {
-    uint32_t r[NC / 32][32];
 #pragma unroll
-    for (int ch = 0; ch < NC / 32; ++ch) tmem_ld32(t_s + ch * 32, r[ch]);
-    tmem_wait_ld_dep(r[0]);
-#pragma unroll
-    for (int ch = 1; ch < NC / 32; ++ch) reg_dep(r[ch]);
-#pragma unroll
-    for (int ch = 0; ch < NC / 32; ++ch)
-#pragma unroll
-      for (int j = 0; j < 32; ++j) s[ch * 32 + j] = __uint_as_float(r[ch][j]);
-  }
+  for (int j = 0; j < NC; ++j) s[j] = __uint_as_float(r[j / 32][j % 32]);
   if (masked) {
 #pragma unroll
     for (int j = 0; j < NC; ++j)
       if (j < lo_c || j > hi_c) s[j] = -INFINITY;
   }
-  float mx = s[0];
+  // row max: 8 independent chains of 3-input maxes, then a small tree
+  float m8[8];
 #pragma unroll
-  for (int j = 1; j < NC; ++j) mx = fmaxf(mx, s[j]);
+  for (int i = 0; i < 8; ++i) m8[i] = s[i];
+#pragma unroll
+  for (int j = 8; j + 16 <= NC; j += 16)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m8[i] = max3(m8[i], s[j + i], s[j + 8 + i]);
+  if ((NC - 8) % 16) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[NC - 8 + i]);
+  }
+  const float mx = fmaxf(max3(m8[0], m8[1], m8[2]),
+                         fmaxf(max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])));
   const float m_tile = mx * c;
   float alpha = 1.0f;
   bool rescale = false;
@@ -191,32 +213,45 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, bool fi
     rescale = true;
   }
   const float m_safe = (m_used == -INFINITY) ? 0.0f : m_used;
-  float sum = 0.0f;
+  const uint64_t cc = f2(c, c);
+  const uint64_t nm = f2(-m_safe, -m_safe);
+  uint64_t acc[4] = {0, 0, 0, 0};  // four packed partial sums (+0.0f bit patterns)
 #pragma unroll
   for (int ch = 0; ch < NC / 32; ++ch) {
     uint32_t pk[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const float p0 = ex2(fmaf(s[ch * 32 + 2 * j], c, -m_safe));
-      const float p1 = ex2(fmaf(s[ch * 32 + 2 * j + 1], c, -m_safe));
-      sum += p0 + p1;
+      const uint64_t x = f2_fma(f2(s[ch * 32 + 2 * j], s[ch * 32 + 2 * j + 1]), cc, nm);
+      float x0, x1;
+      f2_split(x, x0, x1);
+      const float p0 = ex2(x0), p1 = ex2(x1);
+      acc[j & 3] = f2_add(acc[j & 3], f2(p0, p1));
       pk[j] = pack_bf16(p0, p1);
     }
     tmem_st16(t_s + ch * 16, pk);
   }
-  l = l * alpha + sum;
+  const uint64_t acc2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+  float sa, sb;
+  f2_split(acc2, sa, sb);
+  l = l * alpha + (sa + sb);
   // The PV of the previous tile is complete (the commit that signalled this S tile
   // tracks every earlier MMA), and the PV of this tile waits for this warpgroup's P,
   // so O can be rescaled in place here.
   if (__any_sync(0xFFFFFFFFu, rescale)) {
+    const uint64_t aa = f2(alpha, alpha);
 #pragma unroll
     for (int ch = 0; ch < D / 32; ++ch) {
-      uint32_t r[32];
-      tmem_ld32(t_o + ch * 32, r);
-      tmem_wait_ld_dep(r);
+      uint32_t o[32];
+      tmem_ld32(t_o + ch * 32, o);
+      tmem_wait_ld_dep(o);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-      tmem_st32(t_o + ch * 32, r);
+      for (int j = 0; j < 16; ++j) {
+        float lo, hi;
+        f2_split(f2_mul(f2(__uint_as_float(o[2 * j]), __uint_as_float(o[2 * j + 1])), aa), lo, hi);
+        o[2 * j] = __float_as_uint(lo);
+        o[2 * j + 1] = __float_as_uint(hi);
+      }
+      tmem_st32(t_o + ch * 32, o);
     }
   }
   tmem_wait_st();
@@ -270,11 +305,15 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
   wc.abort_flag = &bars->abort_flag;
   wc.err_word = p.err_word;
 
-  const int total_items = __ldg(p.sched + p.num_anchors);
+  const int total_items = __ldg(p.prefix + p.num_anchors);
   const int tok = p.tok_per_tile;
   const int G = p.group;
+  const int stride = gridDim.x;
 
-  if (warp == kWarpProducer) {
+  if (warp >= 8) {
+   // ------------------------------------------------ warpgroup 2: producer, MMA, idle
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+   if (warp == kWarpProducer) {
     if (lane == 0) {
       tma_prefetch_desc(&maps.q);
       tma_prefetch_desc(&maps.k_anc);
@@ -285,22 +324,24 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       uint32_t q_arm[2] = {0, 0}, k_arm[4] = {0, 0, 0, 0}, v_arm[4] = {0, 0, 0, 0};
       bool skip_pending = p.inject_skip_first_kv != 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x, ++it_count) {
-        Item it;
-        decode_item(p, item, it);
-        const int n_tiles = it.n_anchor_tiles + 2 * it.n_sfx_tiles;
+      int item = blockIdx.x;
+      Item it = item < total_items ? load_item(p, item) : Item{};
+      for (; ok && item < total_items; item += stride, ++it_count) {
+        const Item nxt = item + stride < total_items ? load_item(p, item + stride) : it;
+        const int nA = it.n_anchor_tiles();
+        const int n_tiles = nA + 2 * it.n_sfx_tiles();
         for (int pos = 0; pos < n_tiles; ++pos, ++kv_seq) {
           const int slot = kv_seq % C::kStages;
           const uint32_t ph = (kv_seq / C::kStages) & 1u;
           const CUtensorMap* mk;
           const CUtensorMap* mv;
           int row;
-          if (pos < it.n_anchor_tiles) {
+          if (pos < nA) {
             mk = &maps.k_anc;
             mv = &maps.v_anc;
             row = it.a_tok0 + pos * kBN;
           } else {
-            const int rel = pos - it.n_anchor_tiles;
+            const int rel = pos - nA;
             mk = &maps.k_suf;
             mv = &maps.v_suf;
             row = it.ws(rel & 1) + (rel >> 1) * kBN;
@@ -334,6 +375,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           for (int kb = 0; kb < C::kKB; ++kb)
             tma_load_3d(mv, &bars->v_full[slot], v_dst + kb * C::kBlockBytes, kb * 64, it.g, row);
         }
+        it = nxt;
       }
       // Let every load that was issued land before the CTA can exit.
       const uint64_t dl = global_timer_ns() + 100000000ull;
@@ -354,14 +396,17 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       uint32_t kv_base = 0, it_count = 0;
       uint32_t p_cnt[2] = {0, 0};
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x, ++it_count) {
-        Item it;
-        decode_item(p, item, it);
-        const int nA = it.n_anchor_tiles;
-        const int n = nA + it.n_sfx_tiles;
+      int item = blockIdx.x;
+      Item it = item < total_items ? load_item(p, item) : Item{};
+      for (; ok && item < total_items; item += stride, ++it_count) {
+        const Item nxt = item + stride < total_items ? load_item(p, item + stride) : it;
+        const int nA = it.n_anchor_tiles();
+        const int nS = it.n_sfx_tiles();
+        const int nk_sfx = it.nk_sfx();
+        const int n = nA + nS;
 
         auto issue_s = [&](int q, int k) -> bool {
-          const uint32_t seq = kv_base + pos_of(it, q, k);
+          const uint32_t seq = kv_base + pos_of(nA, q, k);
           const int slot = seq % C::kStages;
           const uint32_t ph = (seq / C::kStages) & 1u;
           const bool sfx = k >= nA;
@@ -370,7 +415,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           tc_fence_after();
           const uint32_t kaddr = sKVa + slot * 2 * C::kTileBytes;
           const uint32_t qaddr = sQa + q * C::kTileBytes;
-          const uint32_t idesc = (!sfx || it.nk_sfx == 128) ? kIdescS128 : kIdescS64;
+          const uint32_t idesc = (!sfx || nk_sfx == 128) ? kIdescS128 : kIdescS64;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
@@ -383,7 +428,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           return true;
         };
         auto issue_pv = [&](int q, int k) -> bool {
-          const uint32_t seq = kv_base + pos_of(it, q, k);
+          const uint32_t seq = kv_base + pos_of(nA, q, k);
           const int slot = seq % C::kStages;
           const uint32_t ph = (seq / C::kStages) & 1u;
           const bool sfx = k >= nA;
@@ -392,7 +437,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           ++p_cnt[q];
           tc_fence_after();
           const uint32_t vaddr = sKVa + slot * 2 * C::kTileBytes + C::kTileBytes;
-          const int nk = sfx ? it.nk_sfx : kBN;
+          const int nk = sfx ? nk_sfx : kBN;
           for (int kk = 0; kk < nk / 16; ++kk) {
             mma_ts(tmem + 256u * q + 128u, tmem + 256u * q + 8u * kk,
                    smem_desc_sw128(vaddr + kk * 2048, C::kBlockBytes, 1024), kIdescPV,
@@ -408,14 +453,17 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           ok = issue_pv(0, k) && (k + 1 >= n || issue_s(0, k + 1)) && issue_pv(1, k) &&
                (k + 1 >= n || issue_s(1, k + 1));
         }
-        kv_base += nA + 2 * it.n_sfx_tiles;
+        kv_base += nA + 2 * nS;
+        it = nxt;
       }
       // Every MMA issued so far has completed once this barrier flips.
       mma_commit(&bars->drain);
       drain_wait(&bars->drain, 0, global_timer_ns() + 100000000ull);
     }
+   }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     const int q = warp >> 2;
     const int row = threadIdx.x & 127;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -424,15 +472,18 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
     uint32_t s_cnt = 0, it_count = 0;
     bool ok = true;
     const float c = p.scale_log2;
-    for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x, ++it_count) {
-      Item it;
-      decode_item(p, item, it);
-      const int nA = it.n_anchor_tiles;
-      const int n = nA + it.n_sfx_tiles;
+    int item = blockIdx.x;
+    Item it = item < total_items ? load_item(p, item) : Item{};
+    for (; ok && item < total_items; item += stride, ++it_count) {
+      const Item nxt = item + stride < total_items ? load_item(p, item + stride) : it;
+      const int nA = it.n_anchor_tiles();
+      const int n = nA + it.n_sfx_tiles();
+      const int nk_sfx = it.nk_sfx();
       const int t = it.t0 + q * tok + row / G;
       const bool valid = t < it.tend(q);
-      // visible suffix keys of this row: [vis_lo, t]
-      const int vis_lo = valid ? seg_start(p.suffix_offsets, it.s_lo, it.s_hi, t) : t;
+      // visible suffix keys of this row: [vis_lo, t] (first used on the suffix tiles)
+      const int vis_lo = valid ? __ldg(p.seg + t) : t;
+      const int ws_q = it.ws(q);
       float m_used = -INFINITY, l = 0.0f;
       for (int k = 0; k < n; ++k) {
         if (!(ok = wait_parity(wc, &bars->s_full[q], s_cnt & 1u))) break;
@@ -442,9 +493,9 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           const int rem = it.la - k * kBN;
           softmax_tile<128, D>(t_s, t_o, k == 0, rem < kBN, 0, rem - 1, c, m_used, l);
         } else {
-          const int base = it.ws(q) + (k - nA) * kBN;
+          const int base = ws_q + (k - nA) * kBN;
           const int lo_c = vis_lo - base, hi_c = t - base;
-          if (it.nk_sfx == 64)
+          if (nk_sfx == 64)
             softmax_tile<64, D>(t_s, t_o, k == 0, true, lo_c, hi_c, c, m_used, l);
           else
             softmax_tile<128, D>(t_s, t_o, k == 0, true, lo_c, hi_c, c, m_used, l);
@@ -456,6 +507,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       if (!(ok = wait_parity(wc, &bars->o_done[q], it_count & 1u))) break;
       tc_fence_after();
       const float inv_l = 1.0f / l;
+      const uint64_t il = f2(inv_l, inv_l);
       const int64_t orow = static_cast<int64_t>(t) * p.hq + it.g * G + (row % G);
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + orow * D;
 #pragma unroll
@@ -464,20 +516,23 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         tmem_ld32(t_o + ch * 32, r);
         tmem_wait_ld_dep(r);
         if (valid) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float lo, hi;
+            f2_split(f2_mul(f2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), il),
+                     lo, hi);
+            pk[j] = pack_bf16(lo, hi);
+          }
           uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint4 v;
-            v.x = pack_bf16(__uint_as_float(r[8 * j + 0]) * inv_l, __uint_as_float(r[8 * j + 1]) * inv_l);
-            v.y = pack_bf16(__uint_as_float(r[8 * j + 2]) * inv_l, __uint_as_float(r[8 * j + 3]) * inv_l);
-            v.z = pack_bf16(__uint_as_float(r[8 * j + 4]) * inv_l, __uint_as_float(r[8 * j + 5]) * inv_l);
-            v.w = pack_bf16(__uint_as_float(r[8 * j + 6]) * inv_l, __uint_as_float(r[8 * j + 7]) * inv_l);
-            dst[j] = v;
-          }
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
         }
       }
       if (valid && p.lse != nullptr)
         p.lse[orow] = (m_used + __log2f(l)) * 0.69314718055994531f;
+      it = nxt;
     }
     tc_fence_before();
   }
@@ -491,9 +546,27 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
 }
 
 // ---------------------------------------------------------------------------------
-// Tile schedule: validate the offsets, order anchors by decreasing anchor-tile count
-// (longest work first, so the static round-robin over CTAs approximates LPT) and write
-// the prefix sum of work items over that order.
+// Per-suffix offset checks and the per-token suffix start. Each suffix is checked on its
+// own (0 <= start <= end <= T_S, length <= max_suffix_len) before any write, so nothing
+// outside seg[0, T_S) is ever written; a failed check raises the flag that the schedule
+// kernel turns into QUAIL_ERR_DEVICE_BOUNDS.
+__global__ void __launch_bounds__(256) cascade_segments_kernel(const CascadeParams p) {
+  const int S = p.num_suffixes;
+  const int64_t T = p.total_suffix_tokens;
+  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < S; s += gridDim.x * blockDim.x) {
+    const int lo = __ldg(p.suffix_offsets + s), hi = __ldg(p.suffix_offsets + s + 1);
+    if (lo < 0 || hi < lo || hi > T || hi - lo > p.max_suffix_len) {
+      atomicOr(p.flag, 1);
+      continue;
+    }
+    for (int t = lo; t < hi; ++t) p.seg[t] = lo;
+  }
+}
+
+// Work-item schedule: validate the anchor offsets and the end points, order anchors by
+// decreasing anchor-tile count (longest work first, so the static round-robin over CTAs
+// approximates longest-processing-time-first) and write the prefix sum of work items
+// over that order.
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
@@ -528,15 +601,15 @@ __global__ void __launch_bounds__(1024) cascade_schedule_kernel(const CascadePar
   const int32_t* ao = p.anchor_offsets;
   const int32_t* asp = p.anchor_suffix_ptr;
   const int32_t* so = p.suffix_offsets;
-  int32_t* prefix = p.sched;
-  int32_t* order = p.sched + A + 1;
+  int32_t* prefix = p.prefix;
+  int32_t* order = p.order;
   const int tid = threadIdx.x;
   if (tid == 0) bad = 0;
   for (int i = tid; i < kSortBins; i += blockDim.x) hist[i] = 0;
   __syncthreads();
-  // offsets must be monotone, start at 0, end at the totals, and respect the maxima
   int my_bad = 0;
   if (tid == 0) {
+    my_bad |= *p.flag != 0;  // a per-suffix check failed
     my_bad |= ao[0] != 0 || static_cast<int64_t>(ao[A]) != p.total_anchor_tokens;
     my_bad |= asp[0] != 0 || asp[A] != S;
     my_bad |= so[0] != 0 || static_cast<int64_t>(so[S]) != p.total_suffix_tokens;
@@ -544,10 +617,6 @@ __global__ void __launch_bounds__(1024) cascade_schedule_kernel(const CascadePar
   for (int a = tid; a < A; a += blockDim.x) {
     const int la = ao[a + 1] - ao[a];
     my_bad |= la < 0 || la > p.max_anchor_len || asp[a + 1] < asp[a];
-  }
-  for (int s = tid; s < S; s += blockDim.x) {
-    const int ls = so[s + 1] - so[s];
-    my_bad |= ls < 0 || ls > p.max_suffix_len;
   }
   if (my_bad) atomicOr(&bad, 1);
   __syncthreads();
@@ -574,7 +643,6 @@ __global__ void __launch_bounds__(1024) cascade_schedule_kernel(const CascadePar
     const int pos = atomicAdd(&hist[kSortBins - 1 - key], 1);
     order[pos] = a;
   }
-  __threadfence_block();
   __syncthreads();
   int carry = 0;
   for (int base = 0; base < A; base += blockDim.x) {
@@ -593,25 +661,77 @@ __global__ void __launch_bounds__(1024) cascade_schedule_kernel(const CascadePar
   if (tid == 0) prefix[A] = carry;
 }
 
+// One record per work item: (a_tok0, la, t0, g, ws0, ws1, tend0, tend1).
+__global__ void __launch_bounds__(256) cascade_items_kernel(const CascadeParams p) {
+  const int item = blockIdx.x * blockDim.x + threadIdx.x;
+  const int A = p.num_anchors;
+  const int total = p.prefix[A];
+  if (item >= total) return;
+  int lo = 0, hi = A - 1;  // largest sorted position with prefix <= item
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.prefix[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  const int a = p.order[lo];
+  const int local = item - p.prefix[lo];
+  const int s_begin = p.suffix_offsets[p.anchor_suffix_ptr[a]];
+  const int s_end = p.suffix_offsets[p.anchor_suffix_ptr[a + 1]];
+  const int tok = p.tok_per_tile;
+  const int pairs = (s_end - s_begin + 2 * tok - 1) / (2 * tok);
+  const int g = local / pairs;
+  const int t0 = s_begin + (local % pairs) * 2 * tok;
+  const int tend0 = min(t0 + tok, s_end);
+  const int t1 = t0 + tok;
+  const bool has1 = s_end > t1;
+  int4 r0, r1;
+  r0.x = p.anchor_offsets[a];
+  r0.y = p.anchor_offsets[a + 1] - r0.x;
+  r0.z = t0;
+  r0.w = g;
+  r1.x = p.seg[t0];
+  r1.y = has1 ? p.seg[t1] : t1;
+  r1.z = tend0;
+  r1.w = has1 ? min(t1 + tok, s_end) : t1;
+  int4* dst = reinterpret_cast<int4*>(p.items + 8 * static_cast<int64_t>(item));
+  dst[0] = r0;
+  dst[1] = r1;
+}
+
 }  // namespace
 
-size_t cascade_workspace_bytes(int num_anchors) {
-  const size_t words = 2 * static_cast<size_t>(num_anchors) + 1;
-  return (words * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
+int64_t cascade_item_bound(int num_anchors, int64_t total_suffix_tokens, int hkv, int group) {
+  const int64_t pair_tok = 2 * (128 / group);
+  return static_cast<int64_t>(hkv) * ((total_suffix_tokens + pair_tok - 1) / pair_tok + num_anchors);
+}
+
+CascadeWorkspace cascade_workspace_layout(int num_anchors, int64_t total_suffix_tokens,
+                                          int64_t item_bound) {
+  auto up = [](size_t x, size_t a) { return (x + a - 1) / a * a; };
+  CascadeWorkspace w;
+  w.flag = 0;
+  w.prefix = 16;
+  w.order = w.prefix + 4 * (static_cast<size_t>(num_anchors) + 1);
+  w.seg = up(w.order + 4 * static_cast<size_t>(num_anchors), 16);
+  w.items = up(w.seg + 4 * static_cast<size_t>(total_suffix_tokens), 32);
+  w.total = up(w.items + 32 * static_cast<size_t>(item_bound), 256);
+  return w;
 }
 
 template <int D>
-static cudaError_t launch_cascade_d(const CascadeParams& p, const CascadeMaps& maps,
-                                    int num_sms, cudaStream_t stream) {
+static cudaError_t launch_attn_d(const CascadeParams& p, const CascadeMaps& maps, int num_sms,
+                                 cudaStream_t stream) {
   using C = Cfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(cascade_attn_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmemBytes);
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, cascade_attn_kernel<D>);
   if (e != cudaSuccess) return e;
-  const int64_t pair_tok = 2 * p.tok_per_tile;
-  const int64_t bound =
-      static_cast<int64_t>(p.hkv) * ((p.total_suffix_tokens + pair_tok - 1) / pair_tok + p.num_anchors);
-  const int grid = static_cast<int>(bound < num_sms ? bound : num_sms);
+  // the register split must fit in what the block is launched with (else setmaxnreg.inc
+  // would wait forever)
+  if (static_cast<int64_t>(attr.numRegs) * kThreads < 256 * kRegsSoftmax + 128 * kRegsOther)
+    return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(cascade_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = p.item_bound < num_sms ? p.item_bound : num_sms;
   if (grid <= 0) return cudaSuccess;
   cascade_attn_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(p, maps);
   return cudaGetLastError();
@@ -619,11 +739,22 @@ static cudaError_t launch_cascade_d(const CascadeParams& p, const CascadeMaps& m
 
 cudaError_t launch_cascade(const CascadeParams& p, const CascadeMaps& maps, int head_dim,
                            int num_sms, cudaStream_t stream) {
-  cascade_schedule_kernel<<<1, 1024, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = cudaMemsetAsync(p.flag, 0, sizeof(int32_t), stream);
   if (e != cudaSuccess) return e;
-  if (head_dim == 128) return launch_cascade_d<128>(p, maps, num_sms, stream);
-  return launch_cascade_d<64>(p, maps, num_sms, stream);
+  if (p.num_suffixes > 0) {
+    const int blocks = static_cast<int>(
+        std::min<int64_t>((p.num_suffixes + 255) / 256, static_cast<int64_t>(num_sms) * 8));
+    cascade_segments_kernel<<<blocks, 256, 0, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  cascade_schedule_kernel<<<1, 1024, 0, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (p.item_bound > 0) {
+    cascade_items_kernel<<<(p.item_bound + 255) / 256, 256, 0, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (head_dim == 128) return launch_attn_d<128>(p, maps, num_sms, stream);
+  return launch_attn_d<64>(p, maps, num_sms, stream);
 }
 
 }  // namespace quail

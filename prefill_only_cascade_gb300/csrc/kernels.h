@@ -41,6 +41,7 @@ struct CascadeParams {
   int max_anchor_len, max_suffix_len;
   int hq, hkv, group;        // group = hq / hkv
   int tok_per_tile;          // 128 / group suffix tokens per 128-row query tile
+  int item_bound;            // host-known upper bound of work items
   float scale_log2;          // softmax_scale * log2(e)
   bool fp8;
   const int32_t* anchor_offsets;
@@ -52,18 +53,30 @@ struct CascadeParams {
   const void* v_anc;
   void* out;
   float* lse;
-  int32_t* sched;            // workspace: [A+1] item prefix, then [A] anchor order
+  // workspace (see cascade_workspace_layout)
+  int32_t* flag;             // nonzero: a suffix offset check failed
+  int32_t* prefix;           // [A+1] work-item prefix over the anchor order; [A] = total
+  int32_t* order;            // [A] anchors by decreasing anchor-tile count
+  int32_t* seg;              // [T_S] first token of the suffix that holds each token
+  int32_t* items;            // [item_bound][8] one record per work item
   unsigned* err_word;
   uint64_t timeout_ns;
   int inject_skip_first_kv;
 };
+
+// Byte offsets of the workspace regions; `total` is the size to allocate.
+struct CascadeWorkspace {
+  size_t flag, prefix, order, seg, items, total;
+};
+CascadeWorkspace cascade_workspace_layout(int num_anchors, int64_t total_suffix_tokens,
+                                          int64_t item_bound);
+int64_t cascade_item_bound(int num_anchors, int64_t total_suffix_tokens, int hkv, int group);
 
 // Tensor maps over q_suf, k/v anchor and k/v suffix (bf16, 3-D: d, head, token).
 struct CascadeMaps {
   CUtensorMap q, k_anc, v_anc, k_suf, v_suf;
 };
 
-size_t cascade_workspace_bytes(int num_anchors);
 cudaError_t launch_cascade(const CascadeParams& p, const CascadeMaps& maps, int head_dim,
                            int num_sms, cudaStream_t stream);
 
