@@ -104,6 +104,33 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
 /* Workspace bytes that quail_cascade_attn needs for `desc` (0 when desc is NULL). */
 size_t quail_cascade_workspace_size(const quail_cascade_desc* desc);
 
+/* Size of the library's fixed device scratch array used by quail_cascade_attn_noalloc. */
+#define QUAIL_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * quail_cascade_attn without a caller workspace (no counterpart on the pages: it exists
+ * for callers that must not allocate device memory - e.g. an engine whose device memory
+ * is fixed at start-up, or a plugin host that only passes input and output buffers).
+ * Same arguments, meaning, layouts and checks as quail_cascade_attn, minus `workspace`.
+ * The scratch lives in one file-scope device array of QUAIL_NOALLOC_SCRATCH_BYTES, held
+ * on every GPU that loads the library until the process exits. This call allocates
+ * nothing (no cudaMalloc/cudaFree, no allocating library routine).
+ *   - Returns QUAIL_ERR_UNSUPPORTED when quail_cascade_workspace_size(desc) exceeds
+ *     QUAIL_NOALLOC_SCRATCH_BYTES.
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - Every call uses the same array. Calls whose GPU work overlaps (unordered streams or
+ *     threads) race on it and produce wrong results; order them on one stream.
+ */
+quail_status quail_cascade_attn_noalloc(const quail_cascade_desc* desc, const void* q_suf,
+                                        const void* k_anc, const void* v_anc,
+                                        const void* k_suf, const void* v_suf,
+                                        const int32_t* anchor_offsets,
+                                        const int32_t* anchor_suffix_ptr,
+                                        const int32_t* suffix_offsets, const float* k_scale,
+                                        const float* v_scale, void* out, float* lse,
+                                        quail_stream_t stream);
+
 /*
  * Restricted head of the zero-decode step ([P1] "Como funciona": the final prefill pass
  * emits one token and the output vocabulary is cut to 8 options, shrinking the final

@@ -31,6 +31,7 @@ EXPORTED_SYMBOLS = (
     "quail_cascade_attn", "quail_cascade_workspace_size", "quail_restricted_head",
     "quail_quantize_kv_fp8", "quail_status_string", "quail_get_device_error",
     "quail_set_wait_timeout_ns", "quail_debug_inject", "quail_version",
+    "quail_cascade_attn_noalloc",
 )
 
 
@@ -66,6 +67,9 @@ def _load():
     lib.quail_cascade_attn.argtypes = [ctypes.POINTER(CascadeDesc), vp, vp, vp, vp, vp, i32p,
                                        i32p, i32p, f32p, f32p, vp, f32p, vp, ctypes.c_size_t, vp]
     lib.quail_cascade_attn.restype = ctypes.c_int
+    lib.quail_cascade_attn_noalloc.argtypes = [ctypes.POINTER(CascadeDesc), vp, vp, vp, vp, vp,
+                                               i32p, i32p, i32p, f32p, f32p, vp, f32p, vp]
+    lib.quail_cascade_attn_noalloc.restype = ctypes.c_int
     lib.quail_cascade_workspace_size.argtypes = [ctypes.POINTER(CascadeDesc)]
     lib.quail_cascade_workspace_size.restype = ctypes.c_size_t
     lib.quail_restricted_head.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_float, vp,
@@ -138,6 +142,20 @@ def cascade_attn(desc: CascadeDesc, q_suf, k_anc, v_anc, k_suf, v_suf, anchor_of
         _ptr(v_scale), _ptr(out), _ptr(lse), _ptr(workspace),
         ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(stream))
     _check(st, "quail_cascade_attn")
+
+
+def cascade_attn_noalloc(desc: CascadeDesc, q_suf, k_anc, v_anc, k_suf, v_suf, anchor_offsets,
+                         anchor_suffix_ptr, suffix_offsets, out, lse=None, k_scale=None,
+                         v_scale=None, stream=None):
+    """quail_cascade_attn_noalloc: the same computation with the library's fixed device
+    scratch array instead of a caller workspace (for callers that may not allocate).
+    Calls must not overlap on the GPU; the first call on a device must precede any
+    stream capture."""
+    st = lib.quail_cascade_attn_noalloc(
+        ctypes.byref(desc), _ptr(q_suf), _ptr(k_anc), _ptr(v_anc), _ptr(k_suf), _ptr(v_suf),
+        _ptr(anchor_offsets), _ptr(anchor_suffix_ptr), _ptr(suffix_offsets), _ptr(k_scale),
+        _ptr(v_scale), _ptr(out), _ptr(lse), _stream(stream))
+    _check(st, "quail_cascade_attn_noalloc")
 
 
 def restricted_head(h, gamma, w8, logits, argmax, eps=1e-6, row_index=None, n_rows=None,

@@ -1,0 +1,79 @@
+// noalloc.cu - quail_cascade_attn_noalloc: the cascade attention without a caller
+// workspace, for callers that may not allocate device memory.
+//
+// Some callers cannot call cudaMalloc (or any allocator) around this library: a serving
+// engine whose device memory is carved up once at start-up and may not grow afterwards, a
+// host framework whose plugin interface only hands over input and output buffers, or
+// code on a latency path where an allocation (which can synchronise the device) is not
+// allowed. For them the scratch that the cascade kernels need (offset-check flag, anchor
+// order, work-item prefix, per-token suffix starts and one record per work item) lives in
+// a file-scope device array of fixed size instead of a caller workspace.
+//
+// Cost and limits:
+//   - Every GPU on which the library's kernels are loaded holds kScratchBytes (64 MiB)
+//     for this array until the process exits, whether or not this entry point is used.
+//   - Batches whose scratch would exceed kScratchBytes are rejected with
+//     QUAIL_ERR_UNSUPPORTED (quail_cascade_workspace_size() tells the need).
+//   - All calls share the one array, which keeps the previous call's contents. The only
+//     word that has to start at zero (the offset-check flag) is cleared on the stream by
+//     every call; everything else is written before it is read. Calls whose work
+//     overlaps on the GPU (different streams, or other threads, without ordering) race
+//     on the array and give wrong results.
+//   - The first call on each device looks up the array's device address
+//     (cudaGetSymbolAddress, with that device current); make that first call before any
+//     stream capture begins.
+#include <mutex>
+
+#include "kernels.h"
+#include "quail.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = static_cast<size_t>(QUAIL_NOALLOC_SCRATCH_BYTES);
+static_assert(kScratchBytes % 256 == 0, "scratch size must keep 256-byte alignment");
+
+// In host code this name is only a host-side stand-in for the device array; its device
+// address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_cascade_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+struct ScratchAddr {
+  bool looked_up = false;
+  cudaError_t status = cudaErrorUnknown;
+  void* ptr = nullptr;
+};
+std::mutex g_scratch_mutex;
+ScratchAddr g_scratch[kMaxDevices];
+
+// Device address of the scratch array on the current device (looked up once per device).
+quail_status scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QUAIL_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  ScratchAddr& s = g_scratch[dev];
+  if (!s.looked_up) {
+    s.looked_up = true;
+    s.status = cudaGetSymbolAddress(&s.ptr, g_cascade_scratch);
+  }
+  if (s.status != cudaSuccess || s.ptr == nullptr) return QUAIL_ERR_CUDA;
+  *out = s.ptr;
+  return QUAIL_OK;
+}
+
+}  // namespace
+
+extern "C" quail_status quail_cascade_attn_noalloc(
+    const quail_cascade_desc* desc, const void* q_suf, const void* k_anc, const void* v_anc,
+    const void* k_suf, const void* v_suf, const int32_t* anchor_offsets,
+    const int32_t* anchor_suffix_ptr, const int32_t* suffix_offsets, const float* k_scale,
+    const float* v_scale, void* out, float* lse, quail_stream_t stream) {
+  if (desc == nullptr) return QUAIL_ERR_INVALID_ARG;
+  const size_t need = quail_cascade_workspace_size(desc);
+  if (need > kScratchBytes) return QUAIL_ERR_UNSUPPORTED;  // batch too large for the array
+  void* scratch = nullptr;
+  const quail_status st = scratch_address(&scratch);
+  if (st != QUAIL_OK) return st;
+  return quail_cascade_attn(desc, q_suf, k_anc, v_anc, k_suf, v_suf, anchor_offsets,
+                            anchor_suffix_ptr, suffix_offsets, k_scale, v_scale, out, lse,
+                            scratch, kScratchBytes, stream);
+}
