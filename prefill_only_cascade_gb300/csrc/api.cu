@@ -202,7 +202,6 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
       quail::cascade_workspace_layout(d.num_anchors, d.total_suffix_tokens, item_bound);
   if (workspace == nullptr || workspace_bytes < wl.total || !aligned16(workspace))
     return QUAIL_ERR_INVALID_ARG;
-  if (fp8) return QUAIL_ERR_UNSUPPORTED;  // the FP8 anchor path is not built yet
 
   DeviceState* st = nullptr;
   const quail_status ds = device_state(&st);
@@ -212,11 +211,16 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
   const int D = d.head_dim;
   const int tok = 128 / group;
   quail::CascadeMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  bool ok = encode_3d(&maps.q, q_suf, d.total_suffix_tokens, d.num_q_heads, D, group, tok, bf, 2, 64) &&
-            encode_3d(&maps.k_suf, k_suf, d.total_suffix_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64) &&
-            encode_3d(&maps.v_suf, v_suf, d.total_suffix_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64);
-  if (d.total_anchor_tokens > 0) {
+  // The FP8 variant loads its tiles without TMA; the maps are then unused.
+  bool ok = fp8 ||
+            (encode_3d(&maps.q, q_suf, d.total_suffix_tokens, d.num_q_heads, D, group, tok, bf, 2, 64) &&
+             encode_3d(&maps.k_suf, k_suf, d.total_suffix_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64) &&
+             encode_3d(&maps.v_suf, v_suf, d.total_suffix_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64));
+  if (fp8) {
+    // nothing to encode
+  } else if (d.total_anchor_tokens > 0) {
     ok = ok && encode_3d(&maps.k_anc, k_anc, d.total_anchor_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64) &&
          encode_3d(&maps.v_anc, v_anc, d.total_anchor_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64);
   } else {
@@ -244,8 +248,11 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
   p.suffix_offsets = suffix_offsets;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
+  p.q_suf = q_suf;
   p.k_anc = k_anc;
   p.v_anc = v_anc;
+  p.k_suf = k_suf;
+  p.v_suf = v_suf;
   p.out = out;
   p.lse = lse;
   p.item_bound = static_cast<int>(item_bound);
@@ -261,7 +268,7 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
     p.timeout_ns = g_timeout_ns;
     p.inject_skip_first_kv = g_inject_skip;
   }
-  const cudaError_t e = quail::launch_cascade(p, maps, D, st->num_sms,
+  const cudaError_t e = quail::launch_cascade(p, maps, D, fp8, st->num_sms,
                                               reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QUAIL_OK : QUAIL_ERR_CUDA;
 }

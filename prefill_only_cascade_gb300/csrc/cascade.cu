@@ -34,9 +34,21 @@
 // TMEM (512 columns): tile q uses S/P at columns 256q .. +127 and O at 256q+128 .. +255.
 // The two query tiles share every anchor KV tile loaded into shared memory and ping-pong:
 // while one warpgroup exponentiates its scores the tensor core works on the other tile.
+//
+// FP8 anchor KV (e4m3 codes with one fp32 scale per (anchor, KV head) for K and for V):
+// the same kernel with FP8 = true. tcgen05 kind::f16 needs both operands of one type and
+// there is no exact e4m3 -> bf16 conversion instruction, while e4m3 -> f16 is exact, so
+// this variant runs its MMAs in f16: warps 8, 10 and 11 load every tile with plain
+// 16-byte loads (anchor codes e4m3, Q and suffix K/V bf16), convert to f16 (exact for
+// e4m3; bf16 -> f16 is exact for |x| in [2^-14, 65504] and saturates above) and store it
+// in the same 128-byte-swizzled operand layout that TMA produces. The K scale folds into
+// the score scale of anchor tiles and the V scale into their P (P = p * v_scale, while the
+// row sum keeps p), so O accumulates true values; P is stored as f16.
 #include <algorithm>
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -78,12 +90,13 @@ struct __align__(8) Bars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  int loader_ok;  // FP8 variant: result of the loader leader's wait, read by all loaders
 };
 
 // One work item as written by cascade_items_kernel (two int4).
 struct Item {
   int a_tok0, la;   // anchor token start (into k_anc/v_anc) and length
-  int t0, g;        // first suffix token of query tile 0; KV head
+  int t0, ag;       // first suffix token of query tile 0; anchor * Hkv + KV head
   int ws0, ws1;     // suffix key window start of query tile 0 / 1
   int tend0, tend1; // one past the last valid token of query tile 0 / 1 (tend == start: empty)
   __device__ __forceinline__ int ws(int q) const { return q ? ws1 : ws0; }
@@ -108,7 +121,7 @@ __device__ __forceinline__ Item load_item(const CascadeParams& p, int item) {
   const int4 a = ld_nc_v4(p.items + 8 * static_cast<int64_t>(item));
   const int4 b = ld_nc_v4(p.items + 8 * static_cast<int64_t>(item) + 4);
   Item it;
-  it.a_tok0 = a.x; it.la = a.y; it.t0 = a.z; it.g = a.w;
+  it.a_tok0 = a.x; it.la = a.y; it.t0 = a.z; it.ag = a.w;
   it.ws0 = b.x; it.ws1 = b.y; it.tend0 = b.z; it.tend1 = b.w;
   return it;
 }
@@ -166,14 +179,124 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
+  return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
+}
+
+// ------------------------------------------------------------ FP8-variant tile loaders
+constexpr int kLoaderThreads = 96;  // warps 8, 10, 11
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+      static_cast<__nv_fp8x2_storage_t>(codes16 & 0xFFFFu), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+// Byte offset of 16-byte chunk `jp` (8 f16 / bf16 elements, counted along the row across
+// 64-element blocks) of row r in a 128-byte-swizzled tile of 128-row blocks.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int jp) {
+  return static_cast<uint32_t>((jp >> 3) * 16384 + r * 128 + (((jp & 7) ^ (r & 7)) << 4));
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_nc_u4(const uint8_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ int clamp_rows(int64_t v, int hi) {
+  return v < 0 ? 0 : (v > hi ? hi : static_cast<int>(v));
+}
+__device__ __forceinline__ void loader_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kLoaderThreads) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// bf16 rows -> f16 tile rows [0, rows). Row r of the source starts at
+//   base + (r >> gshift) * tok_stride + (r & (G - 1)) * head_stride  (bytes, d = 128)
+// and rows >= valid_rows read as zero. Done in two halves to bound the loads in flight.
+__device__ __forceinline__ void load_tile_bf16(uint32_t tile, const uint8_t* base,
+                                               int64_t tok_stride, int gshift,
+                                               int64_t head_stride, int rows, int valid_rows,
+                                               int lt) {
+  constexpr int kHalf = (64 * 16 + kLoaderThreads - 1) / kLoaderThreads;
+  const int units = rows * 16;
+  const int gmask = (1 << gshift) - 1;
+#pragma unroll 1
+  for (int h = 0; h < 2; ++h) {
+    uint4 v[kHalf];
+#pragma unroll
+    for (int i = 0; i < kHalf; ++i) {
+      const int u = h * 1024 + lt + i * kLoaderThreads;
+      v[i] = make_uint4(0u, 0u, 0u, 0u);
+      const int r = u >> 4;
+      if (u < min(units, (h + 1) * 1024) && r < valid_rows)
+        v[i] = ld_nc_u4(base + (r >> gshift) * tok_stride + (r & gmask) * head_stride +
+                        (u & 15) * 16);
+    }
+#pragma unroll
+    for (int i = 0; i < kHalf; ++i) {
+      const int u = h * 1024 + lt + i * kLoaderThreads;
+      if (u < min(units, (h + 1) * 1024)) {
+        const uint4 o = make_uint4(bf16x2_to_f16x2(v[i].x), bf16x2_to_f16x2(v[i].y),
+                                   bf16x2_to_f16x2(v[i].z), bf16x2_to_f16x2(v[i].w));
+        st_shared_v4(tile + sw128_offset(u >> 4, u & 15), o);
+      }
+    }
+  }
+}
+
+// e4m3 rows (128 codes each, row r at base + r * row_stride) -> f16 tile; rows >=
+// valid_rows read as zero.
+__device__ __forceinline__ void load_tile_e4m3(uint32_t tile, const uint8_t* base,
+                                               int64_t row_stride, int valid_rows, int lt) {
+  constexpr int kMax = (128 * 8 + kLoaderThreads - 1) / kLoaderThreads;
+  uint4 v[kMax];
+#pragma unroll
+  for (int i = 0; i < kMax; ++i) {
+    const int u = lt + i * kLoaderThreads;
+    v[i] = make_uint4(0u, 0u, 0u, 0u);
+    const int r = u >> 3;
+    if (u < 1024 && r < valid_rows) v[i] = ld_nc_u4(base + r * row_stride + (u & 7) * 16);
+  }
+#pragma unroll
+  for (int i = 0; i < kMax; ++i) {
+    const int u = lt + i * kLoaderThreads;
+    if (u < 1024) {
+      const int r = u >> 3, c = u & 7;  // codes d = 16c .. 16c + 15
+      const uint4 lo = make_uint4(e4m3x2_to_f16x2(v[i].x), e4m3x2_to_f16x2(v[i].x >> 16),
+                                  e4m3x2_to_f16x2(v[i].y), e4m3x2_to_f16x2(v[i].y >> 16));
+      const uint4 hi = make_uint4(e4m3x2_to_f16x2(v[i].z), e4m3x2_to_f16x2(v[i].z >> 16),
+                                  e4m3x2_to_f16x2(v[i].w), e4m3x2_to_f16x2(v[i].w >> 16));
+      st_shared_v4(tile + sw128_offset(r, 2 * c), lo);
+      st_shared_v4(tile + sw128_offset(r, 2 * c + 1), hi);
+    }
+  }
+}
 
 // ---------------------------------------------------------------------------------
 // Softmax of one S tile of NC columns: mask, row max, lazy rescale of O, P = 2^(s c - m)
-// written back to TMEM as bf16 (columns 0 .. NC/2 of the S region), row sum update.
-template <int NC, int D>
+// written back to TMEM as bf16 (f16 times pscale in the FP8 variant) over columns
+// 0 .. NC/2 of the S region, row sum update.
+template <int NC, int D, bool F16P>
 __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, bool first_tile,
                                              bool masked, int lo_c, int hi_c, float c,
-                                             float& m_used, float& l) {
+                                             float pscale, float& m_used, float& l) {
   uint32_t r[NC / 32][32];
 #pragma unroll
   for (int ch = 0; ch < NC / 32; ++ch) tmem_ld32(t_s + ch * 32, r[ch]);
@@ -226,7 +349,11 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, bool fi
       f2_split(x, x0, x1);
       const float p0 = ex2(x0), p1 = ex2(x1);
       acc[j & 3] = f2_add(acc[j & 3], f2(p0, p1));
-      pk[j] = pack_bf16(p0, p1);
+      if (F16P) {
+        pk[j] = pack_p<true>(p0 * pscale, p1 * pscale);  // anchor tiles: P * v_scale
+      } else {
+        pk[j] = pack_p<false>(p0, p1);
+      }
     }
     tmem_st16(t_s + ch * 16, pk);
   }
@@ -258,7 +385,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, bool fi
 }
 
 // ---------------------------------------------------------------------------------
-template <int D>
+template <int D, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
 cascade_attn_kernel(const __grid_constant__ CascadeParams p,
                     const __grid_constant__ CascadeMaps maps) {
@@ -289,6 +416,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
     }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
+    bars->loader_ok = 1;
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -308,12 +436,13 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
   const int total_items = __ldg(p.prefix + p.num_anchors);
   const int tok = p.tok_per_tile;
   const int G = p.group;
+  const int hkv = p.hkv;
   const int stride = gridDim.x;
 
   if (warp >= 8) {
    // ------------------------------------------------ warpgroup 2: producer, MMA, idle
    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
-   if (warp == kWarpProducer) {
+   if (!FP8 && warp == kWarpProducer) {
     if (lane == 0) {
       tma_prefetch_desc(&maps.q);
       tma_prefetch_desc(&maps.k_anc);
@@ -330,6 +459,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         const Item nxt = item + stride < total_items ? load_item(p, item + stride) : it;
         const int nA = it.n_anchor_tiles();
         const int n_tiles = nA + 2 * it.n_sfx_tiles();
+        const int g = it.ag % hkv;
         for (int pos = 0; pos < n_tiles; ++pos, ++kv_seq) {
           const int slot = kv_seq % C::kStages;
           const uint32_t ph = (kv_seq / C::kStages) & 1u;
@@ -355,8 +485,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
             mbar_arrive_expect_tx(&bars->k_full[slot], C::kTileBytes);
             ++k_arm[slot];
             for (int kb = 0; kb < C::kKB; ++kb)
-              tma_load_3d(mk, &bars->k_full[slot], k_dst + kb * C::kBlockBytes, kb * 64, it.g,
-                          row);
+              tma_load_3d(mk, &bars->k_full[slot], k_dst + kb * C::kBlockBytes, kb * 64, g, row);
           }
           if (pos == 0) {
             for (int q = 0; q < 2 && ok; ++q) {
@@ -365,7 +494,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
               ++q_arm[q];
               for (int kb = 0; kb < C::kKB; ++kb)
                 tma_load_3d(&maps.q, &bars->q_full[q], sQ + q * C::kTileBytes + kb * C::kBlockBytes,
-                            kb * 64, it.g * G, it.t0 + q * tok);
+                            kb * 64, g * G, it.t0 + q * tok);
             }
             if (!ok) break;
           }
@@ -373,7 +502,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           mbar_arrive_expect_tx(&bars->v_full[slot], C::kTileBytes);
           ++v_arm[slot];
           for (int kb = 0; kb < C::kKB; ++kb)
-            tma_load_3d(mv, &bars->v_full[slot], v_dst + kb * C::kBlockBytes, kb * 64, it.g, row);
+            tma_load_3d(mv, &bars->v_full[slot], v_dst + kb * C::kBlockBytes, kb * 64, g, row);
         }
         it = nxt;
       }
@@ -386,11 +515,85 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         if (v_arm[s]) drain_wait(&bars->v_full[s], (v_arm[s] - 1) & 1u, dl);
       }
     }
-  } else if (warp == kWarpMma) {
+   } else if (FP8 && warp != kWarpMma) {
+    // ---------------------------------------------- FP8 variant: tile loaders (3 warps)
+    // All 96 threads walk the same job sequence in lockstep. Only the leader waits on an
+    // mbarrier; it publishes the outcome through shared memory across a named barrier,
+    // so an abort is seen by every loader at the same job and none is left at a barrier.
+    const int lt = (warp == kWarpProducer ? 0 : warp - 9) * 32 + lane;
+    volatile int* ok_flag = &bars->loader_ok;
+    const int gshift = __ffs(G) - 1;
+    const uint8_t* q_suf = static_cast<const uint8_t*>(p.q_suf);
+    const int64_t T_S = p.total_suffix_tokens, T_A = p.total_anchor_tokens;
+    bool skip_pending = p.inject_skip_first_kv != 0;
+    auto acquire = [&](uint64_t* bar, uint32_t parity) -> bool {
+      if (lt == 0) *ok_flag = wait_parity(wc, bar, parity) ? 1 : 0;
+      loader_bar();
+      return *ok_flag != 0;
+    };
+    auto publish = [&](uint64_t* bar) {
+      fence_proxy_async();  // the generic-proxy stores must be visible to the tensor core
+      loader_bar();
+      if (lt == 0) mbar_arrive(bar);
+    };
+    uint32_t kv_seq = 0, it_count = 0;
+    bool ok = true;
+    int item = blockIdx.x;
+    Item it = item < total_items ? load_item(p, item) : Item{};
+    for (; ok && item < total_items; item += stride, ++it_count) {
+      const Item nxt = item + stride < total_items ? load_item(p, item + stride) : it;
+      const int nA = it.n_anchor_tiles();
+      const int n_tiles = nA + 2 * it.n_sfx_tiles();
+      const int nk_sfx = it.nk_sfx();
+      const int g = it.ag % hkv;
+      for (int q = 0; q < 2; ++q) {
+        if (!(ok = acquire(&bars->q_empty[q], (it_count & 1u) ^ 1u))) break;
+        const int64_t t0q = it.t0 + q * tok;
+        const int valid = clamp_rows((T_S - t0q) * G, 128);
+        load_tile_bf16(smem_u32(sQ + q * C::kTileBytes),
+                       q_suf + (t0q * p.hq + g * G) * (2 * D), static_cast<int64_t>(p.hq) * 2 * D,
+                       gshift, 2 * D, 128, valid, lt);
+        publish(&bars->q_full[q]);
+      }
+      for (int pos = 0; ok && pos < n_tiles; ++pos, ++kv_seq) {
+        const int slot = kv_seq % C::kStages;
+        const uint32_t ph = (kv_seq / C::kStages) & 1u;
+        for (int w = 0; w < 2; ++w) {  // w = 0: K, w = 1: V
+          uint64_t* empty = w ? &bars->v_empty[slot] : &bars->k_empty[slot];
+          uint64_t* full = w ? &bars->v_full[slot] : &bars->k_full[slot];
+          if (!(ok = acquire(empty, ph ^ 1u))) break;
+          const uint32_t dst = smem_u32(sKV + slot * 2 * C::kTileBytes + w * C::kTileBytes);
+          if (pos < nA) {
+            const int64_t tok0 = it.a_tok0 + pos * kBN;
+            const int valid = clamp_rows(T_A - tok0, 128);
+            const uint8_t* src = static_cast<const uint8_t*>(w ? p.v_anc : p.k_anc);
+            load_tile_e4m3(dst, src + (tok0 * hkv + g) * D, static_cast<int64_t>(hkv) * D,
+                           valid, lt);
+          } else {
+            const int rel = pos - nA;
+            const int64_t tok0 = it.ws(rel & 1) + (rel >> 1) * kBN;
+            const int valid = clamp_rows(T_S - tok0, nk_sfx);
+            const uint8_t* src = static_cast<const uint8_t*>(w ? p.v_suf : p.k_suf);
+            load_tile_bf16(dst, src + (tok0 * hkv + g) * (2 * D),
+                           static_cast<int64_t>(hkv) * 2 * D, 0, 0, nk_sfx, valid, lt);
+          }
+          if (skip_pending) {
+            skip_pending = false;  // fault injection: this tile is never published
+            fence_proxy_async();
+            loader_bar();
+          } else {
+            publish(full);
+          }
+        }
+      }
+      it = nxt;
+    }
+   } else if (warp == kWarpMma) {
     if (lane == 0) {
-      constexpr uint32_t kIdescS128 = idesc_f16(kBM, 128, 1, 0);
-      constexpr uint32_t kIdescS64 = idesc_f16(kBM, 64, 1, 0);
-      constexpr uint32_t kIdescPV = idesc_f16(kBM, D, 1, 1);
+      constexpr uint32_t kAB = FP8 ? 0u : 1u;  // operand type: f16 (FP8 variant) or bf16
+      constexpr uint32_t kIdescS128 = idesc_f16(kBM, 128, kAB, 0);
+      constexpr uint32_t kIdescS64 = idesc_f16(kBM, 64, kAB, 0);
+      constexpr uint32_t kIdescPV = idesc_f16(kBM, D, kAB, 1);
       const uint32_t sQa = smem_u32(sQ);
       const uint32_t sKVa = smem_u32(sKV);
       uint32_t kv_base = 0, it_count = 0;
@@ -479,11 +682,15 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       const int nA = it.n_anchor_tiles();
       const int n = nA + it.n_sfx_tiles();
       const int nk_sfx = it.nk_sfx();
+      const int g = it.ag % hkv;
       const int t = it.t0 + q * tok + row / G;
       const bool valid = t < it.tend(q);
       // visible suffix keys of this row: [vis_lo, t] (first used on the suffix tiles)
       const int vis_lo = valid ? __ldg(p.seg + t) : t;
       const int ws_q = it.ws(q);
+      // FP8 anchor tiles: scores use c * k_scale, and P carries v_scale
+      const float c_anc = FP8 ? c * __ldg(p.k_scale + it.ag) : c;
+      const float v_sc = FP8 ? __ldg(p.v_scale + it.ag) : 1.0f;
       float m_used = -INFINITY, l = 0.0f;
       for (int k = 0; k < n; ++k) {
         if (!(ok = wait_parity(wc, &bars->s_full[q], s_cnt & 1u))) break;
@@ -491,14 +698,15 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         tc_fence_after();
         if (k < nA) {
           const int rem = it.la - k * kBN;
-          softmax_tile<128, D>(t_s, t_o, k == 0, rem < kBN, 0, rem - 1, c, m_used, l);
+          softmax_tile<128, D, FP8>(t_s, t_o, k == 0, rem < kBN, 0, rem - 1, c_anc, v_sc,
+                                    m_used, l);
         } else {
           const int base = ws_q + (k - nA) * kBN;
           const int lo_c = vis_lo - base, hi_c = t - base;
           if (nk_sfx == 64)
-            softmax_tile<64, D>(t_s, t_o, k == 0, true, lo_c, hi_c, c, m_used, l);
+            softmax_tile<64, D, FP8>(t_s, t_o, k == 0, true, lo_c, hi_c, c, 1.0f, m_used, l);
           else
-            softmax_tile<128, D>(t_s, t_o, k == 0, true, lo_c, hi_c, c, m_used, l);
+            softmax_tile<128, D, FP8>(t_s, t_o, k == 0, true, lo_c, hi_c, c, 1.0f, m_used, l);
         }
         tc_fence_before();
         mbar_arrive(&bars->p_full[q]);
@@ -508,7 +716,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       tc_fence_after();
       const float inv_l = 1.0f / l;
       const uint64_t il = f2(inv_l, inv_l);
-      const int64_t orow = static_cast<int64_t>(t) * p.hq + it.g * G + (row % G);
+      const int64_t orow = static_cast<int64_t>(t) * p.hq + g * G + (row % G);
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + orow * D;
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
@@ -661,7 +869,7 @@ __global__ void __launch_bounds__(1024) cascade_schedule_kernel(const CascadePar
   if (tid == 0) prefix[A] = carry;
 }
 
-// One record per work item: (a_tok0, la, t0, g, ws0, ws1, tend0, tend1).
+// One record per work item: (a_tok0, la, t0, a * Hkv + g, ws0, ws1, tend0, tend1).
 __global__ void __launch_bounds__(256) cascade_items_kernel(const CascadeParams p) {
   const int item = blockIdx.x * blockDim.x + threadIdx.x;
   const int A = p.num_anchors;
@@ -687,7 +895,7 @@ __global__ void __launch_bounds__(256) cascade_items_kernel(const CascadeParams 
   r0.x = p.anchor_offsets[a];
   r0.y = p.anchor_offsets[a + 1] - r0.x;
   r0.z = t0;
-  r0.w = g;
+  r0.w = a * p.hkv + g;
   r1.x = p.seg[t0];
   r1.y = has1 ? p.seg[t1] : t1;
   r1.z = tend0;
@@ -717,28 +925,28 @@ CascadeWorkspace cascade_workspace_layout(int num_anchors, int64_t total_suffix_
   return w;
 }
 
-template <int D>
+template <int D, bool FP8>
 static cudaError_t launch_attn_d(const CascadeParams& p, const CascadeMaps& maps, int num_sms,
                                  cudaStream_t stream) {
   using C = Cfg<D>;
   cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, cascade_attn_kernel<D>);
+  cudaError_t e = cudaFuncGetAttributes(&attr, cascade_attn_kernel<D, FP8>);
   if (e != cudaSuccess) return e;
   // the register split must fit in what the block is launched with (else setmaxnreg.inc
   // would wait forever)
   if (static_cast<int64_t>(attr.numRegs) * kThreads < 256 * kRegsSoftmax + 128 * kRegsOther)
     return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(cascade_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           C::kSmemBytes);
+  e = cudaFuncSetAttribute(cascade_attn_kernel<D, FP8>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = p.item_bound < num_sms ? p.item_bound : num_sms;
   if (grid <= 0) return cudaSuccess;
-  cascade_attn_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(p, maps);
+  cascade_attn_kernel<D, FP8><<<grid, kThreads, C::kSmemBytes, stream>>>(p, maps);
   return cudaGetLastError();
 }
 
 cudaError_t launch_cascade(const CascadeParams& p, const CascadeMaps& maps, int head_dim,
-                           int num_sms, cudaStream_t stream) {
+                           bool fp8, int num_sms, cudaStream_t stream) {
   cudaError_t e = cudaMemsetAsync(p.flag, 0, sizeof(int32_t), stream);
   if (e != cudaSuccess) return e;
   if (p.num_suffixes > 0) {
@@ -753,8 +961,9 @@ cudaError_t launch_cascade(const CascadeParams& p, const CascadeMaps& maps, int 
     cascade_items_kernel<<<(p.item_bound + 255) / 256, 256, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (head_dim == 128) return launch_attn_d<128>(p, maps, num_sms, stream);
-  return launch_attn_d<64>(p, maps, num_sms, stream);
+  if (fp8) return launch_attn_d<128, true>(p, maps, num_sms, stream);
+  if (head_dim == 128) return launch_attn_d<128, false>(p, maps, num_sms, stream);
+  return launch_attn_d<64, false>(p, maps, num_sms, stream);
 }
 
 }  // namespace quail

@@ -49,8 +49,11 @@ struct CascadeParams {
   const int32_t* suffix_offsets;
   const float* k_scale;
   const float* v_scale;
-  const void* k_anc;         // raw pointers (the FP8 path reads anchor codes directly)
+  const void* q_suf;         // raw pointers (the FP8 variant loads tiles without TMA)
+  const void* k_anc;
   const void* v_anc;
+  const void* k_suf;
+  const void* v_suf;
   void* out;
   float* lse;
   // workspace (see cascade_workspace_layout)
@@ -78,6 +81,6 @@ struct CascadeMaps {
 };
 
 cudaError_t launch_cascade(const CascadeParams& p, const CascadeMaps& maps, int head_dim,
-                           int num_sms, cudaStream_t stream);
+                           bool fp8, int num_sms, cudaStream_t stream);
 
 }  // namespace quail
