@@ -39,9 +39,12 @@ def parse():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="join", choices=["join", "ragged", "fp8_long"])
+    ap.add_argument("--workload", default="join",
+                    choices=["join", "ragged", "fp8_long", "head", "quantize"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--head-rows", type=int, default=None,
+                    help="fewer rows for --workload head (profiling only)")
     ap.add_argument("--suffixes-per-anchor", type=int, default=None,
                     help="smaller case of the same workload (profiling only)")
     return ap.parse_args()
@@ -433,10 +436,72 @@ def run_e2e(args, q, desc, layout, t, hx, last, k_scale, v_scale, dev, stream, w
             "ms_per_step": ms, "steps": steps}
 
 
+def run_bandwidth_kernel(args):
+    """Per-kernel measurement of the HBM-bound kernels (not the headline step):
+    --workload head      restricted head on 2,000,000 rows x 2,560 (bf16)
+    --workload quantize  E4M3 quantisation of the long-anchor workload's anchor K
+    Prints one JSON line with the kernel's CUDA-event time and its HBM roofline."""
+    import prefill_only_cascade_gb300 as q
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    pk, src = peaks()
+    if args.workload == "head":
+        cfg = workloads.HEAD_CONFIGS["head"]
+        n = args.head_rows or cfg.num_rows
+        x = workloads.make_head_inputs(cfg, dev, num_rows=n)
+        logits = torch.empty(n, 8, dtype=torch.float32, device=dev)
+        am = torch.empty(n, dtype=torch.int32, device=dev)
+        run = lambda: q.restricted_head(x["h"], x["gamma"], x["w8"], logits, am, eps=cfg.eps,
+                                        stream=stream)
+        algo_bytes = n * (cfg.hidden * 2 + 8 * 4 + 4) + cfg.hidden * 2 * 9
+        units, unit = n, "rows/s"
+        kernel = "restricted_head_kernel"
+    else:
+        cfg = workloads.ATTN_CONFIGS["fp8_long"]
+        lay = workloads.make_layout(cfg)
+        g = torch.Generator(device=dev).manual_seed(4)
+        kv = workloads._randn_bf16((lay.total_anchor_tokens, cfg.num_kv_heads, cfg.head_dim), g, dev)
+        codes = torch.empty(kv.shape, dtype=torch.uint8, device=dev)
+        scale = torch.empty(cfg.num_anchors, cfg.num_kv_heads, dtype=torch.float32, device=dev)
+        ao = torch.from_numpy(lay.anchor_offsets.copy()).to(dev)
+        run = lambda: q.quantize_kv_fp8(kv, ao, codes, scale, stream=stream)
+        algo_bytes = kv.numel() * 3 + scale.numel() * 4
+        units, unit = kv.numel(), "elements/s"
+        kernel = "kv_amax_kernel + kv_quantize_kernel + amax_to_scale_kernel"
+    for _ in range(max(args.warmup, 3)):
+        run()
+    torch.cuda.synchronize()
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    with ClockSampler(0) as clk:
+        time.sleep(0.3)
+        for a, b in evs:
+            flush.zero_()  # evict L2 (larger than L2) between timed launches
+            a.record(stream)
+            run()
+            b.record(stream)
+        torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    gbs = algo_bytes / (ms / 1e3) / 1e9
+    line = {"metric": f"{args.workload} kernel throughput", "value": units / (ms / 1e3),
+            "unit": unit, "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": ms, "higher_is_better": True, "data": "synthetic",
+            "config": {"workload": args.workload, "l2": "flushed between launches"},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
+                         "peak_source": f"hbm_gbs of {src}", "kernel": kernel,
+                         "algorithmic_bytes_per_launch": algo_bytes},
+            "clocks": clk.summary()}
+    print(json.dumps(line))
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload in ("head", "quantize"):
+        run_bandwidth_kernel(args)
     else:
         run_ours(args)
 
