@@ -60,12 +60,10 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kThreads = 384;             // three warpgroups
-// Register split (setmaxnreg): the two softmax warpgroups grow to kRegsSoftmax, the
-// producer/MMA warpgroup shrinks to kRegsOther. 256 * 184 + 128 * 136 = 64,512 registers,
-// which must not exceed the 384 * (registers at launch) the block holds; the host checks
-// the compiled register count before launching.
-constexpr int kRegsSoftmax = 184;
-constexpr int kRegsOther = 136;
+// Register split (setmaxnreg): the two softmax warpgroups grow to Cfg::kRegsSoftmax, the
+// producer/MMA warpgroup shrinks to Cfg::kRegsOther; 256 * softmax + 128 * other =
+// 64,512 registers, which must not exceed the 384 * (registers at launch) the block
+// holds; the host checks the compiled register count before launching.
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: O is rescaled only past 2^8
@@ -81,6 +79,9 @@ struct Cfg {
   static constexpr int kSmemQ = 2 * kTileBytes;
   static constexpr int kSmemKV = kStages * 2 * kTileBytes;
   static constexpr int kSmemBytes = kSmemQ + kSmemKV + 1024 + 1024;
+  static constexpr int kRegsSoftmax = (D == 128) ? 176 : 184;
+  static constexpr int kRegsOther = (D == 128) ? 152 : 136;
+  static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= 384 * 168, "register split");
 };
 
 struct __align__(8) Bars {
@@ -405,7 +406,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       mbar_init(&bars->q_full[q], 1);
       mbar_init(&bars->q_empty[q], 1);
       mbar_init(&bars->s_full[q], 1);
-      mbar_init(&bars->p_full[q], kBM);
+      mbar_init(&bars->p_full[q], 4);  // one arrival per softmax warp
       mbar_init(&bars->o_done[q], 1);
     }
     for (int s = 0; s < C::kStages; ++s) {
@@ -441,7 +442,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
 
   if (warp >= 8) {
    // ------------------------------------------------ warpgroup 2: producer, MMA, idle
-   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsOther));
    if (!FP8 && warp == kWarpProducer) {
     if (lane == 0) {
       tma_prefetch_desc(&maps.q);
@@ -594,8 +595,11 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       constexpr uint32_t kIdescS128 = idesc_f16(kBM, 128, kAB, 0);
       constexpr uint32_t kIdescS64 = idesc_f16(kBM, 64, kAB, 0);
       constexpr uint32_t kIdescPV = idesc_f16(kBM, D, kAB, 1);
-      const uint32_t sQa = smem_u32(sQ);
-      const uint32_t sKVa = smem_u32(sKV);
+      constexpr uint32_t kDescHi = sw128_desc_hi(1024);  // 8-row groups 1024 bytes apart
+      const uint32_t q_lo0 = sw128_desc_lo(smem_u32(sQ), 16);
+      const uint32_t k_lo0 = sw128_desc_lo(smem_u32(sKV), 16);
+      // V is the MN-major B operand: 64-column blocks (128 rows x 128 bytes) 16 KB apart
+      const uint32_t v_lo0 = sw128_desc_lo(smem_u32(sKV + C::kTileBytes), C::kBlockBytes);
       uint32_t kv_base = 0, it_count = 0;
       uint32_t p_cnt[2] = {0, 0};
       bool ok = true;
@@ -616,14 +620,15 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           if ((sfx || q == 0) && !wait_parity(wc, &bars->k_full[slot], ph)) return false;
           if (k == 0 && !wait_parity(wc, &bars->q_full[q], it_count & 1u)) return false;
           tc_fence_after();
-          const uint32_t kaddr = sKVa + slot * 2 * C::kTileBytes;
-          const uint32_t qaddr = sQa + q * C::kTileBytes;
+          const uint32_t k_lo = k_lo0 + slot * (2 * C::kTileBytes >> 4);
+          const uint32_t q_lo = q_lo0 + q * (C::kTileBytes >> 4);
           const uint32_t idesc = (!sfx || nk_sfx == 128) ? kIdescS128 : kIdescS64;
+          const uint32_t d_s = tmem + 256u * q;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-            mma_ss(tmem + 256u * q, smem_desc_sw128(qaddr + off, 16, 1024),
-                   smem_desc_sw128(kaddr + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+            // K step kk: 128-byte block kk / 4, 32-byte column offset (kk % 4) inside it
+            const uint32_t adv = (kk >> 2) * (C::kBlockBytes >> 4) + (kk & 3) * 2;
+            mma_ss_lohi(d_s, q_lo + adv, kDescHi, k_lo + adv, kDescHi, idesc, kk > 0 ? 1u : 0u);
           }
           mma_commit(&bars->s_full[q]);
           if (sfx || q == 1) mma_commit(&bars->k_empty[slot]);
@@ -639,12 +644,18 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           if (!wait_parity(wc, &bars->p_full[q], p_cnt[q] & 1u)) return false;
           ++p_cnt[q];
           tc_fence_after();
-          const uint32_t vaddr = sKVa + slot * 2 * C::kTileBytes + C::kTileBytes;
-          const int nk = sfx ? nk_sfx : kBN;
-          for (int kk = 0; kk < nk / 16; ++kk) {
-            mma_ts(tmem + 256u * q + 128u, tmem + 256u * q + 8u * kk,
-                   smem_desc_sw128(vaddr + kk * 2048, C::kBlockBytes, 1024), kIdescPV,
-                   (k > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t v_lo = v_lo0 + slot * (2 * C::kTileBytes >> 4);
+          const uint32_t d_o = tmem + 256u * q + 128u;
+          const uint32_t a_p = tmem + 256u * q;
+          const uint32_t acc0 = k > 0 ? 1u : 0u;
+          // 16 keys per step: 16 rows of 128 bytes of V; P columns advance by 8 (2 x bf16)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts_lohi(d_o, a_p + 8u * kk, v_lo + kk * 128, kDescHi, kIdescPV, kk > 0 ? 1u : acc0);
+          if (!sfx || nk_sfx == 128) {
+#pragma unroll
+            for (int kk = 4; kk < 8; ++kk)
+              mma_ts_lohi(d_o, a_p + 8u * kk, v_lo + kk * 128, kDescHi, kIdescPV, 1u);
           }
           if (sfx || q == 1) mma_commit(&bars->v_empty[slot]);
           if (k == n - 1) mma_commit(&bars->o_done[q]);
@@ -666,7 +677,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
    }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsSoftmax));
     const int q = warp >> 2;
     const int row = threadIdx.x & 127;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -709,7 +720,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
             softmax_tile<128, D, FP8>(t_s, t_o, k == 0, true, lo_c, hi_c, c, 1.0f, m_used, l);
         }
         tc_fence_before();
-        mbar_arrive(&bars->p_full[q]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full[q]);
       }
       if (!ok) break;
       if (!(ok = wait_parity(wc, &bars->o_done[q], it_count & 1u))) break;
@@ -934,7 +946,7 @@ static cudaError_t launch_attn_d(const CascadeParams& p, const CascadeMaps& maps
   if (e != cudaSuccess) return e;
   // the register split must fit in what the block is launched with (else setmaxnreg.inc
   // would wait forever)
-  if (static_cast<int64_t>(attr.numRegs) * kThreads < 256 * kRegsSoftmax + 128 * kRegsOther)
+  if (static_cast<int64_t>(attr.numRegs) * kThreads < 256 * C::kRegsSoftmax + 128 * C::kRegsOther)
     return cudaErrorInvalidConfiguration;
   e = cudaFuncSetAttribute(cascade_attn_kernel<D, FP8>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
