@@ -444,12 +444,17 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
    // ------------------------------------------------ warpgroup 2: producer, MMA, idle
    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsOther));
    if (!FP8 && warp == kWarpProducer) {
-    if (lane == 0) {
-      tma_prefetch_desc(&maps.q);
-      tma_prefetch_desc(&maps.k_anc);
-      tma_prefetch_desc(&maps.v_anc);
-      tma_prefetch_desc(&maps.k_suf);
-      tma_prefetch_desc(&maps.v_suf);
+    // The whole warp walks the schedule (so every operand is warp-uniform); one elected
+    // lane issues the TMA copies and the expect-tx arrivals.
+    {
+      const bool leader = elect_one();
+      if (leader) {
+        tma_prefetch_desc(&maps.q);
+        tma_prefetch_desc(&maps.k_anc);
+        tma_prefetch_desc(&maps.v_anc);
+        tma_prefetch_desc(&maps.k_suf);
+        tma_prefetch_desc(&maps.v_suf);
+      }
       uint32_t kv_seq = 0, it_count = 0;
       uint32_t q_arm[2] = {0, 0}, k_arm[4] = {0, 0, 0, 0}, v_arm[4] = {0, 0, 0, 0};
       bool skip_pending = p.inject_skip_first_kv != 0;
@@ -479,31 +484,41 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           }
           uint8_t* k_dst = sKV + slot * 2 * C::kTileBytes;
           uint8_t* v_dst = k_dst + C::kTileBytes;
-          if (!(ok = wait_parity(wc, &bars->k_empty[slot], ph ^ 1u))) break;
+          if (!(ok = wait_parity_warp(wc, &bars->k_empty[slot], ph ^ 1u))) break;
           if (skip_pending) {
             skip_pending = false;  // fault injection: this tile's K never arrives
           } else {
-            mbar_arrive_expect_tx(&bars->k_full[slot], C::kTileBytes);
             ++k_arm[slot];
-            for (int kb = 0; kb < C::kKB; ++kb)
-              tma_load_3d(mk, &bars->k_full[slot], k_dst + kb * C::kBlockBytes, kb * 64, g, row);
+            if (leader) {
+              mbar_arrive_expect_tx(&bars->k_full[slot], C::kTileBytes);
+              for (int kb = 0; kb < C::kKB; ++kb)
+                tma_load_3d(mk, &bars->k_full[slot], k_dst + kb * C::kBlockBytes, kb * 64, g, row);
+            }
+            __syncwarp();
           }
           if (pos == 0) {
             for (int q = 0; q < 2 && ok; ++q) {
-              if (!(ok = wait_parity(wc, &bars->q_empty[q], (it_count & 1u) ^ 1u))) break;
-              mbar_arrive_expect_tx(&bars->q_full[q], C::kTileBytes);
+              if (!(ok = wait_parity_warp(wc, &bars->q_empty[q], (it_count & 1u) ^ 1u))) break;
               ++q_arm[q];
-              for (int kb = 0; kb < C::kKB; ++kb)
-                tma_load_3d(&maps.q, &bars->q_full[q], sQ + q * C::kTileBytes + kb * C::kBlockBytes,
-                            kb * 64, g * G, it.t0 + q * tok);
+              if (leader) {
+                mbar_arrive_expect_tx(&bars->q_full[q], C::kTileBytes);
+                for (int kb = 0; kb < C::kKB; ++kb)
+                  tma_load_3d(&maps.q, &bars->q_full[q],
+                              sQ + q * C::kTileBytes + kb * C::kBlockBytes, kb * 64, g * G,
+                              it.t0 + q * tok);
+              }
+              __syncwarp();
             }
             if (!ok) break;
           }
-          if (!(ok = wait_parity(wc, &bars->v_empty[slot], ph ^ 1u))) break;
-          mbar_arrive_expect_tx(&bars->v_full[slot], C::kTileBytes);
+          if (!(ok = wait_parity_warp(wc, &bars->v_empty[slot], ph ^ 1u))) break;
           ++v_arm[slot];
-          for (int kb = 0; kb < C::kKB; ++kb)
-            tma_load_3d(mv, &bars->v_full[slot], v_dst + kb * C::kBlockBytes, kb * 64, g, row);
+          if (leader) {
+            mbar_arrive_expect_tx(&bars->v_full[slot], C::kTileBytes);
+            for (int kb = 0; kb < C::kKB; ++kb)
+              tma_load_3d(mv, &bars->v_full[slot], v_dst + kb * C::kBlockBytes, kb * 64, g, row);
+          }
+          __syncwarp();
         }
         it = nxt;
       }
@@ -590,7 +605,9 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       it = nxt;
     }
    } else if (warp == kWarpMma) {
-    if (lane == 0) {
+    // Whole warp walks the schedule; one elected lane issues tcgen05.mma / commit.
+    {
+      const bool leader = elect_one();
       constexpr uint32_t kAB = FP8 ? 0u : 1u;  // operand type: f16 (FP8 variant) or bf16
       constexpr uint32_t kIdescS128 = idesc_f16(kBM, 128, kAB, 0);
       constexpr uint32_t kIdescS64 = idesc_f16(kBM, 64, kAB, 0);
@@ -617,22 +634,25 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           const int slot = seq % C::kStages;
           const uint32_t ph = (seq / C::kStages) & 1u;
           const bool sfx = k >= nA;
-          if ((sfx || q == 0) && !wait_parity(wc, &bars->k_full[slot], ph)) return false;
-          if (k == 0 && !wait_parity(wc, &bars->q_full[q], it_count & 1u)) return false;
+          if ((sfx || q == 0) && !wait_parity_warp(wc, &bars->k_full[slot], ph)) return false;
+          if (k == 0 && !wait_parity_warp(wc, &bars->q_full[q], it_count & 1u)) return false;
           tc_fence_after();
           const uint32_t k_lo = k_lo0 + slot * (2 * C::kTileBytes >> 4);
           const uint32_t q_lo = q_lo0 + q * (C::kTileBytes >> 4);
           const uint32_t idesc = (!sfx || nk_sfx == 128) ? kIdescS128 : kIdescS64;
           const uint32_t d_s = tmem + 256u * q;
+          if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            // K step kk: 128-byte block kk / 4, 32-byte column offset (kk % 4) inside it
-            const uint32_t adv = (kk >> 2) * (C::kBlockBytes >> 4) + (kk & 3) * 2;
-            mma_ss_lohi(d_s, q_lo + adv, kDescHi, k_lo + adv, kDescHi, idesc, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              // K step kk: 128-byte block kk / 4, 32-byte column offset (kk % 4) inside it
+              const uint32_t adv = (kk >> 2) * (C::kBlockBytes >> 4) + (kk & 3) * 2;
+              mma_ss_lohi(d_s, q_lo + adv, kDescHi, k_lo + adv, kDescHi, idesc, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bars->s_full[q]);
+            if (sfx || q == 1) mma_commit(&bars->k_empty[slot]);
+            if (k == n - 1) mma_commit(&bars->q_empty[q]);
           }
-          mma_commit(&bars->s_full[q]);
-          if (sfx || q == 1) mma_commit(&bars->k_empty[slot]);
-          if (k == n - 1) mma_commit(&bars->q_empty[q]);
+          __syncwarp();
           return true;
         };
         auto issue_pv = [&](int q, int k) -> bool {
@@ -640,25 +660,30 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           const int slot = seq % C::kStages;
           const uint32_t ph = (seq / C::kStages) & 1u;
           const bool sfx = k >= nA;
-          if ((sfx || q == 0) && !wait_parity(wc, &bars->v_full[slot], ph)) return false;
-          if (!wait_parity(wc, &bars->p_full[q], p_cnt[q] & 1u)) return false;
+          if ((sfx || q == 0) && !wait_parity_warp(wc, &bars->v_full[slot], ph)) return false;
+          if (!wait_parity_warp(wc, &bars->p_full[q], p_cnt[q] & 1u)) return false;
           ++p_cnt[q];
           tc_fence_after();
           const uint32_t v_lo = v_lo0 + slot * (2 * C::kTileBytes >> 4);
           const uint32_t d_o = tmem + 256u * q + 128u;
           const uint32_t a_p = tmem + 256u * q;
           const uint32_t acc0 = k > 0 ? 1u : 0u;
-          // 16 keys per step: 16 rows of 128 bytes of V; P columns advance by 8 (2 x bf16)
+          const bool full = !sfx || nk_sfx == 128;
+          if (leader) {
+            // 16 keys per step: 16 rows of 128 bytes of V; P columns advance by 8 (2 x bf16)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ts_lohi(d_o, a_p + 8u * kk, v_lo + kk * 128, kDescHi, kIdescPV, kk > 0 ? 1u : acc0);
-          if (!sfx || nk_sfx == 128) {
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts_lohi(d_o, a_p + 8u * kk, v_lo + kk * 128, kDescHi, kIdescPV,
+                          kk > 0 ? 1u : acc0);
+            if (full) {
 #pragma unroll
-            for (int kk = 4; kk < 8; ++kk)
-              mma_ts_lohi(d_o, a_p + 8u * kk, v_lo + kk * 128, kDescHi, kIdescPV, 1u);
+              for (int kk = 4; kk < 8; ++kk)
+                mma_ts_lohi(d_o, a_p + 8u * kk, v_lo + kk * 128, kDescHi, kIdescPV, 1u);
+            }
+            if (sfx || q == 1) mma_commit(&bars->v_empty[slot]);
+            if (k == n - 1) mma_commit(&bars->o_done[q]);
           }
-          if (sfx || q == 1) mma_commit(&bars->v_empty[slot]);
-          if (k == n - 1) mma_commit(&bars->o_done[q]);
+          __syncwarp();
           return true;
         };
 
@@ -671,7 +696,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         it = nxt;
       }
       // Every MMA issued so far has completed once this barrier flips.
-      mma_commit(&bars->drain);
+      if (leader) mma_commit(&bars->drain);
+      __syncwarp();
       drain_wait(&bars->drain, 0, global_timer_ns() + 100000000ull);
     }
    }

@@ -79,6 +79,23 @@ __device__ __forceinline__ bool wait_parity(const WaitCtl& w, uint64_t* bar, uin
   }
 }
 
+// One lane of a converged warp (the same lane every time the warp is converged).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// wait_parity by every lane of a converged warp; true only if every lane saw completion.
+__device__ __forceinline__ bool wait_parity_warp(const WaitCtl& w, uint64_t* bar,
+                                                 uint32_t parity) {
+  return __all_sync(0xFFFFFFFFu, wait_parity(w, bar, parity));
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
