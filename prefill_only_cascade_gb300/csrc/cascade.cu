@@ -629,33 +629,19 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         const int nk_sfx = it.nk_sfx();
         const int n = nA + nS;
 
-        auto issue_s = [&](int q, int k) -> bool {
+        // Waits (K fill, Q fill) for S(q, k) and (V fill, P ready) for PV(q, k); the MMAs
+        // are issued only after every wait of the next pair of groups is done, so PV(q, k)
+        // and S(q, k + 1) go to the tensor pipe back to back.
+        auto wait_s = [&](int q, int k) -> bool {
           const uint32_t seq = kv_base + pos_of(nA, q, k);
           const int slot = seq % C::kStages;
           const uint32_t ph = (seq / C::kStages) & 1u;
           const bool sfx = k >= nA;
           if ((sfx || q == 0) && !wait_parity_warp(wc, &bars->k_full[slot], ph)) return false;
           if (k == 0 && !wait_parity_warp(wc, &bars->q_full[q], it_count & 1u)) return false;
-          tc_fence_after();
-          const uint32_t k_lo = k_lo0 + slot * (2 * C::kTileBytes >> 4);
-          const uint32_t q_lo = q_lo0 + q * (C::kTileBytes >> 4);
-          const uint32_t idesc = (!sfx || nk_sfx == 128) ? kIdescS128 : kIdescS64;
-          const uint32_t d_s = tmem + 256u * q;
-          if (leader) {
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              // K step kk: 128-byte block kk / 4, 32-byte column offset (kk % 4) inside it
-              const uint32_t adv = (kk >> 2) * (C::kBlockBytes >> 4) + (kk & 3) * 2;
-              mma_ss_lohi(d_s, q_lo + adv, kDescHi, k_lo + adv, kDescHi, idesc, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&bars->s_full[q]);
-            if (sfx || q == 1) mma_commit(&bars->k_empty[slot]);
-            if (k == n - 1) mma_commit(&bars->q_empty[q]);
-          }
-          __syncwarp();
           return true;
         };
-        auto issue_pv = [&](int q, int k) -> bool {
+        auto wait_pv = [&](int q, int k) -> bool {
           const uint32_t seq = kv_base + pos_of(nA, q, k);
           const int slot = seq % C::kStages;
           const uint32_t ph = (seq / C::kStages) & 1u;
@@ -663,34 +649,68 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           if ((sfx || q == 0) && !wait_parity_warp(wc, &bars->v_full[slot], ph)) return false;
           if (!wait_parity_warp(wc, &bars->p_full[q], p_cnt[q] & 1u)) return false;
           ++p_cnt[q];
-          tc_fence_after();
+          return true;
+        };
+        // Issue parts: called by the elected lane only.
+        auto mma_s = [&](int q, int k) {
+          const uint32_t seq = kv_base + pos_of(nA, q, k);
+          const int slot = seq % C::kStages;
+          const bool sfx = k >= nA;
+          const uint32_t k_lo = k_lo0 + slot * (2 * C::kTileBytes >> 4);
+          const uint32_t q_lo = q_lo0 + q * (C::kTileBytes >> 4);
+          const uint32_t idesc = (!sfx || nk_sfx == 128) ? kIdescS128 : kIdescS64;
+          const uint32_t d_s = tmem + 256u * q;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            // K step kk: 128-byte block kk / 4, 32-byte column offset (kk % 4) inside it
+            const uint32_t adv = (kk >> 2) * (C::kBlockBytes >> 4) + (kk & 3) * 2;
+            mma_ss_lohi(d_s, q_lo + adv, kDescHi, k_lo + adv, kDescHi, idesc, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars->s_full[q]);
+          if (sfx || q == 1) mma_commit(&bars->k_empty[slot]);
+          if (k == n - 1) mma_commit(&bars->q_empty[q]);
+        };
+        auto mma_pv = [&](int q, int k) {
+          const uint32_t seq = kv_base + pos_of(nA, q, k);
+          const int slot = seq % C::kStages;
+          const bool sfx = k >= nA;
           const uint32_t v_lo = v_lo0 + slot * (2 * C::kTileBytes >> 4);
           const uint32_t d_o = tmem + 256u * q + 128u;
           const uint32_t a_p = tmem + 256u * q;
           const uint32_t acc0 = k > 0 ? 1u : 0u;
-          const bool full = !sfx || nk_sfx == 128;
-          if (leader) {
-            // 16 keys per step: 16 rows of 128 bytes of V; P columns advance by 8 (2 x bf16)
+          // 16 keys per step: 16 rows of 128 bytes of V; P columns advance by 8 (2 x bf16)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ts_lohi(d_o, a_p + 8u * kk, v_lo + kk * 128, kDescHi, kIdescPV,
-                          kk > 0 ? 1u : acc0);
-            if (full) {
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts_lohi(d_o, a_p + 8u * kk, v_lo + kk * 128, kDescHi, kIdescPV, kk > 0 ? 1u : acc0);
+          if (!sfx || nk_sfx == 128) {
 #pragma unroll
-              for (int kk = 4; kk < 8; ++kk)
-                mma_ts_lohi(d_o, a_p + 8u * kk, v_lo + kk * 128, kDescHi, kIdescPV, 1u);
-            }
-            if (sfx || q == 1) mma_commit(&bars->v_empty[slot]);
-            if (k == n - 1) mma_commit(&bars->o_done[q]);
+            for (int kk = 4; kk < 8; ++kk)
+              mma_ts_lohi(d_o, a_p + 8u * kk, v_lo + kk * 128, kDescHi, kIdescPV, 1u);
           }
-          __syncwarp();
-          return true;
+          if (sfx || q == 1) mma_commit(&bars->v_empty[slot]);
+          if (k == n - 1) mma_commit(&bars->o_done[q]);
         };
 
-        ok = issue_s(0, 0) && issue_s(1, 0);
+        ok = wait_s(0, 0) && wait_s(1, 0);
+        if (ok) {
+          tc_fence_after();
+          if (leader) {
+            mma_s(0, 0);
+            mma_s(1, 0);
+          }
+          __syncwarp();
+        }
         for (int k = 0; ok && k < n; ++k) {
-          ok = issue_pv(0, k) && (k + 1 >= n || issue_s(0, k + 1)) && issue_pv(1, k) &&
-               (k + 1 >= n || issue_s(1, k + 1));
+          for (int q = 0; q < 2 && ok; ++q) {
+            ok = wait_pv(q, k) && (k + 1 >= n || wait_s(q, k + 1));
+            if (!ok) break;
+            tc_fence_after();
+            if (leader) {
+              mma_pv(q, k);
+              if (k + 1 < n) mma_s(q, k + 1);
+            }
+            __syncwarp();
+          }
         }
         kv_base += nA + 2 * nS;
         it = nxt;
