@@ -84,7 +84,7 @@ typedef struct {
  *   suffix_offsets    [S+1] int32 token prefix sums into q_suf/k_suf/v_suf/out/lse
  *   k_scale, v_scale  [A, Hkv] fp32 dequantisation scales (value = e4m3(code) * scale);
  *                     required for FP8_E4M3, must be NULL for BF16
- *   out     [T_S, Hq, d] bf16 (round to nearest even from fp32)
+ *   out     [T_S, Hq, d] bf16 (round to nearest even from fp32), 32-byte aligned
  *   lse     [T_S, Hq] fp32 natural log of the sum of exp(scaled scores); may be NULL
  *   workspace: device scratch of at least quail_cascade_workspace_size(desc) bytes,
  *              16-byte aligned; its contents are overwritten. Calls that share one

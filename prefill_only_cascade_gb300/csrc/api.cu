@@ -184,7 +184,8 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
   if (d.total_suffix_tokens > 0) {
     if (q_suf == nullptr || k_suf == nullptr || v_suf == nullptr || out == nullptr)
       return QUAIL_ERR_INVALID_ARG;
-    if (!aligned16(q_suf) || !aligned16(k_suf) || !aligned16(v_suf) || !aligned16(out))
+    if (!aligned16(q_suf) || !aligned16(k_suf) || !aligned16(v_suf) ||
+        (reinterpret_cast<uintptr_t>(out) & 31u))  // out rows are written with 32-byte stores
       return QUAIL_ERR_INVALID_ARG;
   }
   if (d.total_anchor_tokens > 0) {

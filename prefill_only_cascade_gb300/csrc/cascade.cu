@@ -221,6 +221,12 @@ __device__ __forceinline__ uint4 ld_nc_u4(const uint8_t* p) {
 __device__ __forceinline__ int clamp_rows(int64_t v, int hi) {
   return v < 0 ? 0 : (v > hi ? hi : static_cast<int>(v));
 }
+// 32-byte global store (sm_100+); p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
 __device__ __forceinline__ void loader_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(kLoaderThreads) : "memory");
 }
@@ -776,24 +782,30 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       const uint64_t il = f2(inv_l, inv_l);
       const int64_t orow = static_cast<int64_t>(t) * p.hq + g * G + (row % G);
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + orow * D;
+      // Two 32-column chunks of O per TMEM wait; each thread writes its row with 32-byte
+      // stores (one full sector each).
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(t_o + ch * 32, r);
-        tmem_wait_ld_dep(r);
+      for (int ch2 = 0; ch2 < D / 64; ++ch2) {
+        uint32_t r[2][32];
+        tmem_ld32(t_o + ch2 * 64, r[0]);
+        tmem_ld32(t_o + ch2 * 64 + 32, r[1]);
+        tmem_wait_ld_dep(r[0]);
+        reg_dep(r[1]);
         if (valid) {
-          uint32_t pk[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float lo, hi;
-            f2_split(f2_mul(f2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), il),
-                     lo, hi);
-            pk[j] = pack_bf16(lo, hi);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              float lo, hi;
+              f2_split(f2_mul(f2(__uint_as_float(r[h][2 * j]), __uint_as_float(r[h][2 * j + 1])),
+                              il),
+                       lo, hi);
+              pk[j] = pack_bf16(lo, hi);
+            }
+            st_global_v8(out + ch2 * 64 + h * 32, pk);
+            st_global_v8(out + ch2 * 64 + h * 32 + 16, pk + 8);
           }
-          uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
         }
       }
       if (valid && p.lse != nullptr)

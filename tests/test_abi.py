@@ -87,6 +87,7 @@ def test_cascade_rejects_bad_pointers():
     assert _call_attn(None) == q.QUAIL_ERR_INVALID_ARG
     assert _call_attn(d, q_suf=None) == q.QUAIL_ERR_INVALID_ARG
     assert _call_attn(d, out=0x10008) == q.QUAIL_ERR_INVALID_ARG          # not 16-byte aligned
+    assert _call_attn(d, out=0x10010) == q.QUAIL_ERR_INVALID_ARG          # not 32-byte aligned
     assert _call_attn(d, so=None) == q.QUAIL_ERR_INVALID_ARG
     assert _call_attn(d, ws=None) == q.QUAIL_ERR_INVALID_ARG
     assert _call_attn(d, ws_bytes=8) == q.QUAIL_ERR_INVALID_ARG           # workspace too small
