@@ -110,18 +110,40 @@ restricted_head_kernel(int64_t n_rows, int hidden, float eps, const __nv_bfloat1
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float ssA = 0.f, ssB = 0.f;
     const uint4 zero = make_uint4(0, 0, 0, 0);
-#pragma unroll 4
-    for (int c = 0; c < nchunks; ++c) {
-      const uint4 a = okA ? ld_stream_16(pA + 32 * c) : zero;
-      const uint4 b = okB ? ld_stream_16(pB + 32 * c) : zero;
-      const uint4 wh = whi[c * 32 + lane];
-      const uint4 wl = wlo[c * 32 + lane];
-      mma_bf16_16816(acc, a.x, b.x, a.y, b.y, wh.x, wh.y);
-      mma_bf16_16816(acc, a.z, b.z, a.w, b.w, wh.z, wh.w);
-      mma_bf16_16816(acc, a.x, b.x, a.y, b.y, wl.x, wl.y);
-      mma_bf16_16816(acc, a.z, b.z, a.w, b.w, wl.z, wl.w);
-      ssA = sq_sum_bf16x8(a, ssA);
-      ssB = sq_sum_bf16x8(b, ssB);
+    // Software pipeline over batches of kB chunks with two register buffers: the loads of
+    // the next batch are in flight while the current batch is multiplied.
+    constexpr int kB = 4;
+    uint4 xa[2][kB], xb[2][kB];
+    auto load = [&](int buf, int c0) {
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
+        const bool in = c0 + i < nchunks;
+        xa[buf][i] = (okA && in) ? ld_stream_16(pA + 32 * (c0 + i)) : zero;
+        xb[buf][i] = (okB && in) ? ld_stream_16(pB + 32 * (c0 + i)) : zero;
+      }
+    };
+    auto compute = [&](int buf, int c0) {
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
+        if (c0 + i < nchunks) {
+          const uint4 a = xa[buf][i], b = xb[buf][i];
+          const uint4 wh = whi[(c0 + i) * 32 + lane];
+          const uint4 wl = wlo[(c0 + i) * 32 + lane];
+          mma_bf16_16816(acc, a.x, b.x, a.y, b.y, wh.x, wh.y);
+          mma_bf16_16816(acc, a.z, b.z, a.w, b.w, wh.z, wh.w);
+          mma_bf16_16816(acc, a.x, b.x, a.y, b.y, wl.x, wl.y);
+          mma_bf16_16816(acc, a.z, b.z, a.w, b.w, wl.z, wl.w);
+          ssA = sq_sum_bf16x8(a, ssA);
+          ssB = sq_sum_bf16x8(b, ssB);
+        }
+      }
+    };
+    load(0, 0);
+    for (int c = 0; c < nchunks; c += 2 * kB) {
+      if (c + kB < nchunks) load(1, c + kB);
+      compute(0, c);
+      if (c + 2 * kB < nchunks) load(0, c + 2 * kB);
+      if (c + kB < nchunks) compute(1, c + kB);
     }
     // The four lanes of a quad share rows g and g + 8.
     ssA += __shfl_xor_sync(0xFFFFFFFFu, ssA, 1);
