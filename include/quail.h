@@ -158,7 +158,7 @@ quail_status quail_restricted_head(int64_t n_rows, int32_t hidden, float eps, co
  *   and all d; code = e4m3(x / scale), x / scale rounded to fp32 first, then rounded to
  *   nearest even with saturation at +-448 (sign kept).
  *   kv_bf16 [T_A, Hkv, d] bf16 in; kv_e4m3 [T_A, Hkv, d] codes out; scale [A, Hkv] fp32
- *   out. d in {64, 128}. A memset and three small kernels on `stream`.
+ *   out. d in {64, 128}, Hkv * d <= 4096. A memset and three small kernels on `stream`.
  */
 quail_status quail_quantize_kv_fp8(int32_t num_anchors, const int32_t* anchor_offsets,
                                    int64_t total_anchor_tokens, int32_t num_kv_heads,

@@ -307,6 +307,7 @@ quail_status quail_quantize_kv_fp8(int32_t num_anchors, const int32_t* anchor_of
       num_kv_heads <= 0)
     return QUAIL_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return QUAIL_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(num_kv_heads) * head_dim > 4096) return QUAIL_ERR_UNSUPPORTED;
   if (num_anchors == 0 && total_anchor_tokens != 0) return QUAIL_ERR_INVALID_ARG;
   if (num_anchors > 0 && (anchor_offsets == nullptr || scale == nullptr)) return QUAIL_ERR_INVALID_ARG;
   if (total_anchor_tokens > 0 &&

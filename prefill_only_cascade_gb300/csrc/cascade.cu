@@ -268,21 +268,24 @@ __device__ __forceinline__ void load_tile_bf16(uint32_t tile, const uint8_t* bas
   }
 }
 
-// e4m3 rows (128 codes each, row r at base + r * row_stride) -> f16 tile; rows >=
+// e4m3 rows (128 codes each, row r at base + r * row_stride) -> f16 tile, in two phases so
+// that the loads of one tile can be in flight while another tile is converted: rows >=
 // valid_rows read as zero.
-__device__ __forceinline__ void load_tile_e4m3(uint32_t tile, const uint8_t* base,
+constexpr int kE4m3PerThread = (128 * 8 + kLoaderThreads - 1) / kLoaderThreads;
+__device__ __forceinline__ void load_e4m3_regs(uint4 (&v)[kE4m3PerThread], const uint8_t* base,
                                                int64_t row_stride, int valid_rows, int lt) {
-  constexpr int kMax = (128 * 8 + kLoaderThreads - 1) / kLoaderThreads;
-  uint4 v[kMax];
 #pragma unroll
-  for (int i = 0; i < kMax; ++i) {
+  for (int i = 0; i < kE4m3PerThread; ++i) {
     const int u = lt + i * kLoaderThreads;
     v[i] = make_uint4(0u, 0u, 0u, 0u);
     const int r = u >> 3;
     if (u < 1024 && r < valid_rows) v[i] = ld_nc_u4(base + r * row_stride + (u & 7) * 16);
   }
+}
+__device__ __forceinline__ void store_e4m3_regs(uint32_t tile, const uint4 (&v)[kE4m3PerThread],
+                                                int lt) {
 #pragma unroll
-  for (int i = 0; i < kMax; ++i) {
+  for (int i = 0; i < kE4m3PerThread; ++i) {
     const int u = lt + i * kLoaderThreads;
     if (u < 1024) {
       const int r = u >> 3, c = u & 7;  // codes d = 16c .. 16c + 15
@@ -577,34 +580,56 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
                        gshift, 2 * D, 128, valid, lt);
         publish(&bars->q_full[q]);
       }
+      // Anchor tiles (e4m3): K and V of one tile alternate between two register buffers so
+      // the next job's loads are in flight while the current job is converted.
+      const uint8_t* k_src = static_cast<const uint8_t*>(p.k_anc);
+      const uint8_t* v_src = static_cast<const uint8_t*>(p.v_anc);
+      auto anc_base = [&](const uint8_t* src, int t) {
+        return src + (static_cast<int64_t>(it.a_tok0 + t * kBN) * hkv + g) * D;
+      };
+      auto anc_valid = [&](int t) { return clamp_rows(T_A - (it.a_tok0 + t * kBN), 128); };
+      const int64_t anc_stride = static_cast<int64_t>(hkv) * D;
+      uint4 kbuf[kE4m3PerThread], vbuf[kE4m3PerThread];
+      if (nA > 0) load_e4m3_regs(kbuf, anc_base(k_src, 0), anc_stride, anc_valid(0), lt);
       for (int pos = 0; ok && pos < n_tiles; ++pos, ++kv_seq) {
         const int slot = kv_seq % C::kStages;
         const uint32_t ph = (kv_seq / C::kStages) & 1u;
-        for (int w = 0; w < 2; ++w) {  // w = 0: K, w = 1: V
-          uint64_t* empty = w ? &bars->v_empty[slot] : &bars->k_empty[slot];
-          uint64_t* full = w ? &bars->v_full[slot] : &bars->k_full[slot];
-          if (!(ok = acquire(empty, ph ^ 1u))) break;
-          const uint32_t dst = smem_u32(sKV + slot * 2 * C::kTileBytes + w * C::kTileBytes);
-          if (pos < nA) {
-            const int64_t tok0 = it.a_tok0 + pos * kBN;
-            const int valid = clamp_rows(T_A - tok0, 128);
-            const uint8_t* src = static_cast<const uint8_t*>(w ? p.v_anc : p.k_anc);
-            load_tile_e4m3(dst, src + (tok0 * hkv + g) * D, static_cast<int64_t>(hkv) * D,
-                           valid, lt);
-          } else {
-            const int rel = pos - nA;
-            const int64_t tok0 = it.ws(rel & 1) + (rel >> 1) * kBN;
-            const int valid = clamp_rows(T_S - tok0, nk_sfx);
-            const uint8_t* src = static_cast<const uint8_t*>(w ? p.v_suf : p.k_suf);
-            load_tile_bf16(dst, src + (tok0 * hkv + g) * (2 * D),
-                           static_cast<int64_t>(hkv) * 2 * D, 0, 0, nk_sfx, valid, lt);
-          }
+        const uint32_t k_dst = smem_u32(sKV + slot * 2 * C::kTileBytes);
+        const uint32_t v_dst = k_dst + C::kTileBytes;
+        if (pos < nA) {
+          load_e4m3_regs(vbuf, anc_base(v_src, pos), anc_stride, anc_valid(pos), lt);
+          if (!(ok = acquire(&bars->k_empty[slot], ph ^ 1u))) break;
+          store_e4m3_regs(k_dst, kbuf, lt);
           if (skip_pending) {
             skip_pending = false;  // fault injection: this tile is never published
             fence_proxy_async();
             loader_bar();
           } else {
-            publish(full);
+            publish(&bars->k_full[slot]);
+          }
+          if (pos + 1 < nA)
+            load_e4m3_regs(kbuf, anc_base(k_src, pos + 1), anc_stride, anc_valid(pos + 1), lt);
+          if (!(ok = acquire(&bars->v_empty[slot], ph ^ 1u))) break;
+          store_e4m3_regs(v_dst, vbuf, lt);
+          publish(&bars->v_full[slot]);
+        } else {
+          const int rel = pos - nA;
+          const int64_t tok0 = it.ws(rel & 1) + (rel >> 1) * kBN;
+          const int valid = clamp_rows(T_S - tok0, nk_sfx);
+          for (int w = 0; w < 2 && ok; ++w) {  // w = 0: K, w = 1: V
+            uint64_t* empty = w ? &bars->v_empty[slot] : &bars->k_empty[slot];
+            uint64_t* full = w ? &bars->v_full[slot] : &bars->k_full[slot];
+            if (!(ok = acquire(empty, ph ^ 1u))) break;
+            const uint8_t* src = static_cast<const uint8_t*>(w ? p.v_suf : p.k_suf);
+            load_tile_bf16(w ? v_dst : k_dst, src + (tok0 * hkv + g) * (2 * D),
+                           static_cast<int64_t>(hkv) * 2 * D, 0, 0, nk_sfx, valid, lt);
+            if (skip_pending) {
+              skip_pending = false;
+              fence_proxy_async();
+              loader_bar();
+            } else {
+              publish(full);
+            }
           }
         }
       }
