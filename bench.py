@@ -164,13 +164,31 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(world, value: float) -> float:
+def max_over_ranks(world, value: float, device="cuda") -> float:
+    """Largest value over the ranks (the job's time is its slowest rank's time)."""
     if world == 1:
         return value
     import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    t = torch.tensor([value], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def sum_over_ranks(world, value: float, device="cuda") -> float:
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_workload(cfg, rank: int):
+    """Weak scaling: every rank gets its own batch of the same shape (independent anchors
+    with their suffixes; nothing is exchanged between ranks), drawn with a rank-specific
+    seed."""
+    import dataclasses
+    return dataclasses.replace(cfg, seed=cfg.seed + 7919 * rank) if rank else cfg
 
 
 # ---------------------------------------------------------------------------- oracle timing
@@ -271,6 +289,7 @@ def run_ours(args):
     cfg = workloads.ATTN_CONFIGS[args.workload]
     if args.suffixes_per_anchor:
         cfg = dataclasses.replace(cfg, suffixes_per_anchor=args.suffixes_per_anchor)
+    cfg = rank_workload(cfg, rank)
     layout = workloads.make_layout(cfg)
     hq, hkv, d = cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim
     t = workloads.make_attention_inputs(cfg, layout, dev)
@@ -334,7 +353,7 @@ def run_ours(args):
     if q.get_device_error() != q.QUAIL_OK:
         raise RuntimeError("device error during the timed region")
     ms_per_step = elapsed_ms / args.steps
-    tokens = layout.total_suffix_tokens * world
+    tokens = sum_over_ranks(world, float(layout.total_suffix_tokens))
     value = tokens / (ms_per_step / 1e3)
 
     pk, src = peaks()
@@ -431,7 +450,8 @@ def run_e2e(args, q, desc, layout, t, hx, last, k_scale, v_scale, dev, stream, w
     ms = max_over_ranks(world, a.elapsed_time(b)) / steps
     del dev_in, h_dev, out
     torch.cuda.empty_cache()
-    return {"value": layout.total_suffix_tokens * world / (ms / 1e3), "unit": "suffix tokens/s",
+    return {"value": sum_over_ranks(world, float(layout.total_suffix_tokens)) / (ms / 1e3),
+            "unit": "suffix tokens/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": ms, "steps": steps}
 

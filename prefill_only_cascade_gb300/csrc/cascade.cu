@@ -211,11 +211,11 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                "r"(v.z), "r"(v.w)
                : "memory");
 }
-__device__ __forceinline__ uint4 ld_nc_u4(const uint8_t* p) {
+__device__ __forceinline__ uint4 ld_nc_u4(const uint8_t* p, uint64_t policy) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+               : "l"(p), "l"(policy));
   return v;
 }
 __device__ __forceinline__ int clamp_rows(int64_t v, int hi) {
@@ -240,7 +240,7 @@ __device__ __forceinline__ void fence_proxy_async() {
 __device__ __forceinline__ void load_tile_bf16(uint32_t tile, const uint8_t* base,
                                                int64_t tok_stride, int gshift,
                                                int64_t head_stride, int rows, int valid_rows,
-                                               int lt) {
+                                               int lt, uint64_t policy) {
   constexpr int kHalf = (64 * 16 + kLoaderThreads - 1) / kLoaderThreads;
   const int units = rows * 16;
   const int gmask = (1 << gshift) - 1;
@@ -254,7 +254,7 @@ __device__ __forceinline__ void load_tile_bf16(uint32_t tile, const uint8_t* bas
       const int r = u >> 4;
       if (u < min(units, (h + 1) * 1024) && r < valid_rows)
         v[i] = ld_nc_u4(base + (r >> gshift) * tok_stride + (r & gmask) * head_stride +
-                        (u & 15) * 16);
+                        (u & 15) * 16, policy);
     }
 #pragma unroll
     for (int i = 0; i < kHalf; ++i) {
@@ -273,13 +273,14 @@ __device__ __forceinline__ void load_tile_bf16(uint32_t tile, const uint8_t* bas
 // valid_rows read as zero.
 constexpr int kE4m3PerThread = (128 * 8 + kLoaderThreads - 1) / kLoaderThreads;
 __device__ __forceinline__ void load_e4m3_regs(uint4 (&v)[kE4m3PerThread], const uint8_t* base,
-                                               int64_t row_stride, int valid_rows, int lt) {
+                                               int64_t row_stride, int valid_rows, int lt,
+                                               uint64_t policy) {
 #pragma unroll
   for (int i = 0; i < kE4m3PerThread; ++i) {
     const int u = lt + i * kLoaderThreads;
     v[i] = make_uint4(0u, 0u, 0u, 0u);
     const int r = u >> 3;
-    if (u < 1024 && r < valid_rows) v[i] = ld_nc_u4(base + r * row_stride + (u & 7) * 16);
+    if (u < 1024 && r < valid_rows) v[i] = ld_nc_u4(base + r * row_stride + (u & 7) * 16, policy);
   }
 }
 __device__ __forceinline__ void store_e4m3_regs(uint32_t tile, const uint4 (&v)[kE4m3PerThread],
@@ -464,6 +465,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         tma_prefetch_desc(&maps.k_suf);
         tma_prefetch_desc(&maps.v_suf);
       }
+      const uint64_t keep = l2_policy_evict_last(), stream_pol = l2_policy_evict_first();
       uint32_t kv_seq = 0, it_count = 0;
       uint32_t q_arm[2] = {0, 0}, k_arm[4] = {0, 0, 0, 0}, v_arm[4] = {0, 0, 0, 0};
       bool skip_pending = p.inject_skip_first_kv != 0;
@@ -481,15 +483,18 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           const CUtensorMap* mk;
           const CUtensorMap* mv;
           int row;
+          uint64_t pol;
           if (pos < nA) {
             mk = &maps.k_anc;
             mv = &maps.v_anc;
             row = it.a_tok0 + pos * kBN;
+            pol = keep;
           } else {
             const int rel = pos - nA;
             mk = &maps.k_suf;
             mv = &maps.v_suf;
             row = it.ws(rel & 1) + (rel >> 1) * kBN;
+            pol = stream_pol;
           }
           uint8_t* k_dst = sKV + slot * 2 * C::kTileBytes;
           uint8_t* v_dst = k_dst + C::kTileBytes;
@@ -501,7 +506,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
             if (leader) {
               mbar_arrive_expect_tx(&bars->k_full[slot], C::kTileBytes);
               for (int kb = 0; kb < C::kKB; ++kb)
-                tma_load_3d(mk, &bars->k_full[slot], k_dst + kb * C::kBlockBytes, kb * 64, g, row);
+                tma_load_3d_hint(mk, &bars->k_full[slot], k_dst + kb * C::kBlockBytes, kb * 64, g,
+                                 row, pol);
             }
             __syncwarp();
           }
@@ -512,9 +518,9 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
               if (leader) {
                 mbar_arrive_expect_tx(&bars->q_full[q], C::kTileBytes);
                 for (int kb = 0; kb < C::kKB; ++kb)
-                  tma_load_3d(&maps.q, &bars->q_full[q],
-                              sQ + q * C::kTileBytes + kb * C::kBlockBytes, kb * 64, g * G,
-                              it.t0 + q * tok);
+                  tma_load_3d_hint(&maps.q, &bars->q_full[q],
+                                   sQ + q * C::kTileBytes + kb * C::kBlockBytes, kb * 64, g * G,
+                                   it.t0 + q * tok, stream_pol);
               }
               __syncwarp();
             }
@@ -525,7 +531,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           if (leader) {
             mbar_arrive_expect_tx(&bars->v_full[slot], C::kTileBytes);
             for (int kb = 0; kb < C::kKB; ++kb)
-              tma_load_3d(mv, &bars->v_full[slot], v_dst + kb * C::kBlockBytes, kb * 64, g, row);
+              tma_load_3d_hint(mv, &bars->v_full[slot], v_dst + kb * C::kBlockBytes, kb * 64, g,
+                               row, pol);
           }
           __syncwarp();
         }
@@ -550,6 +557,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
     const int gshift = __ffs(G) - 1;
     const uint8_t* q_suf = static_cast<const uint8_t*>(p.q_suf);
     const int64_t T_S = p.total_suffix_tokens, T_A = p.total_anchor_tokens;
+    const uint64_t keep = l2_policy_evict_last(), stream_pol = l2_policy_evict_first();
     bool skip_pending = p.inject_skip_first_kv != 0;
     auto acquire = [&](uint64_t* bar, uint32_t parity) -> bool {
       if (lt == 0) *ok_flag = wait_parity(wc, bar, parity) ? 1 : 0;
@@ -577,7 +585,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         const int valid = clamp_rows((T_S - t0q) * G, 128);
         load_tile_bf16(smem_u32(sQ + q * C::kTileBytes),
                        q_suf + (t0q * p.hq + g * G) * (2 * D), static_cast<int64_t>(p.hq) * 2 * D,
-                       gshift, 2 * D, 128, valid, lt);
+                       gshift, 2 * D, 128, valid, lt, stream_pol);
         publish(&bars->q_full[q]);
       }
       // Anchor tiles (e4m3): K and V of one tile alternate between two register buffers so
@@ -590,14 +598,14 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       auto anc_valid = [&](int t) { return clamp_rows(T_A - (it.a_tok0 + t * kBN), 128); };
       const int64_t anc_stride = static_cast<int64_t>(hkv) * D;
       uint4 kbuf[kE4m3PerThread], vbuf[kE4m3PerThread];
-      if (nA > 0) load_e4m3_regs(kbuf, anc_base(k_src, 0), anc_stride, anc_valid(0), lt);
+      if (nA > 0) load_e4m3_regs(kbuf, anc_base(k_src, 0), anc_stride, anc_valid(0), lt, keep);
       for (int pos = 0; ok && pos < n_tiles; ++pos, ++kv_seq) {
         const int slot = kv_seq % C::kStages;
         const uint32_t ph = (kv_seq / C::kStages) & 1u;
         const uint32_t k_dst = smem_u32(sKV + slot * 2 * C::kTileBytes);
         const uint32_t v_dst = k_dst + C::kTileBytes;
         if (pos < nA) {
-          load_e4m3_regs(vbuf, anc_base(v_src, pos), anc_stride, anc_valid(pos), lt);
+          load_e4m3_regs(vbuf, anc_base(v_src, pos), anc_stride, anc_valid(pos), lt, keep);
           if (!(ok = acquire(&bars->k_empty[slot], ph ^ 1u))) break;
           store_e4m3_regs(k_dst, kbuf, lt);
           if (skip_pending) {
@@ -608,7 +616,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
             publish(&bars->k_full[slot]);
           }
           if (pos + 1 < nA)
-            load_e4m3_regs(kbuf, anc_base(k_src, pos + 1), anc_stride, anc_valid(pos + 1), lt);
+            load_e4m3_regs(kbuf, anc_base(k_src, pos + 1), anc_stride, anc_valid(pos + 1), lt,
+                           keep);
           if (!(ok = acquire(&bars->v_empty[slot], ph ^ 1u))) break;
           store_e4m3_regs(v_dst, vbuf, lt);
           publish(&bars->v_full[slot]);
@@ -622,7 +631,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
             if (!(ok = acquire(empty, ph ^ 1u))) break;
             const uint8_t* src = static_cast<const uint8_t*>(w ? p.v_suf : p.k_suf);
             load_tile_bf16(w ? v_dst : k_dst, src + (tok0 * hkv + g) * (2 * D),
-                           static_cast<int64_t>(hkv) * 2 * D, 0, 0, nk_sfx, valid, lt);
+                           static_cast<int64_t>(hkv) * 2 * D, 0, 0, nk_sfx, valid, lt, stream_pol);
             if (skip_pending) {
               skip_pending = false;
               fence_proxy_async();
