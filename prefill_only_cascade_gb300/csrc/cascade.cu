@@ -83,6 +83,13 @@ struct Cfg {
   static constexpr int kRegsOther = (D == 128) ? 152 : 136;
   static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= 384 * 168, "register split");
 };
+// The FP8 variant's loader warps (in the third warpgroup) need more registers.
+template <int D, bool FP8>
+struct Regs {
+  static constexpr int kSoftmax = FP8 ? 168 : Cfg<D>::kRegsSoftmax;
+  static constexpr int kOther = FP8 ? 168 : Cfg<D>::kRegsOther;
+  static_assert(256 * kSoftmax + 128 * kOther <= 384 * 168, "register split");
+};
 
 struct __align__(8) Bars {
   uint64_t q_full[2], q_empty[2];
@@ -196,10 +203,15 @@ constexpr int kLoaderThreads = 96;  // warps 8, 10, 11
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
-      static_cast<__nv_fp8x2_storage_t>(codes16 & 0xFFFFu), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// Four e4m3 codes (bytes 0..3 of w) -> two f16x2 words (codes 0,1 and codes 2,3; the lower
+// code in the lower half). Exact: every e4m3 value is an f16 value.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& a, uint32_t& b) {
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(a), "=r"(b)
+      : "r"(w));
 }
 // Byte offset of 16-byte chunk `jp` (8 f16 / bf16 elements, counted along the row across
 // 64-element blocks) of row r in a 128-byte-swizzled tile of 128-row blocks.
@@ -271,7 +283,13 @@ __device__ __forceinline__ void load_tile_bf16(uint32_t tile, const uint8_t* bas
 // e4m3 rows (128 codes each, row r at base + r * row_stride) -> f16 tile, in two phases so
 // that the loads of one tile can be in flight while another tile is converted: rows >=
 // valid_rows read as zero.
+//
+// Unit u (16 codes) -> row and 16-code column c chosen so that the 32 lanes of one warp
+// instruction cover 8 rows x 4 columns: with the 128-byte swizzle their 16-byte stores then
+// spread evenly over the 8 bank groups (4 lanes each, the minimum for 512 bytes).
 constexpr int kE4m3PerThread = (128 * 8 + kLoaderThreads - 1) / kLoaderThreads;
+__device__ __forceinline__ int e4m3_row(int u) { return (u >> 6) * 8 + ((u & 31) >> 2); }
+__device__ __forceinline__ int e4m3_col(int u) { return (u & 3) + 4 * ((u >> 5) & 1); }
 __device__ __forceinline__ void load_e4m3_regs(uint4 (&v)[kE4m3PerThread], const uint8_t* base,
                                                int64_t row_stride, int valid_rows, int lt,
                                                uint64_t policy) {
@@ -279,8 +297,9 @@ __device__ __forceinline__ void load_e4m3_regs(uint4 (&v)[kE4m3PerThread], const
   for (int i = 0; i < kE4m3PerThread; ++i) {
     const int u = lt + i * kLoaderThreads;
     v[i] = make_uint4(0u, 0u, 0u, 0u);
-    const int r = u >> 3;
-    if (u < 1024 && r < valid_rows) v[i] = ld_nc_u4(base + r * row_stride + (u & 7) * 16, policy);
+    const int r = e4m3_row(u);
+    if (u < 1024 && r < valid_rows)
+      v[i] = ld_nc_u4(base + r * row_stride + e4m3_col(u) * 16, policy);
   }
 }
 __device__ __forceinline__ void store_e4m3_regs(uint32_t tile, const uint4 (&v)[kE4m3PerThread],
@@ -289,11 +308,12 @@ __device__ __forceinline__ void store_e4m3_regs(uint32_t tile, const uint4 (&v)[
   for (int i = 0; i < kE4m3PerThread; ++i) {
     const int u = lt + i * kLoaderThreads;
     if (u < 1024) {
-      const int r = u >> 3, c = u & 7;  // codes d = 16c .. 16c + 15
-      const uint4 lo = make_uint4(e4m3x2_to_f16x2(v[i].x), e4m3x2_to_f16x2(v[i].x >> 16),
-                                  e4m3x2_to_f16x2(v[i].y), e4m3x2_to_f16x2(v[i].y >> 16));
-      const uint4 hi = make_uint4(e4m3x2_to_f16x2(v[i].z), e4m3x2_to_f16x2(v[i].z >> 16),
-                                  e4m3x2_to_f16x2(v[i].w), e4m3x2_to_f16x2(v[i].w >> 16));
+      const int r = e4m3_row(u), c = e4m3_col(u);  // codes d = 16c .. 16c + 15
+      uint4 lo, hi;
+      e4m3x4_to_f16x4(v[i].x, lo.x, lo.y);
+      e4m3x4_to_f16x4(v[i].y, lo.z, lo.w);
+      e4m3x4_to_f16x4(v[i].z, hi.x, hi.y);
+      e4m3x4_to_f16x4(v[i].w, hi.z, hi.w);
       st_shared_v4(tile + sw128_offset(r, 2 * c), lo);
       st_shared_v4(tile + sw128_offset(r, 2 * c + 1), hi);
     }
@@ -452,7 +472,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
 
   if (warp >= 8) {
    // ------------------------------------------------ warpgroup 2: producer, MMA, idle
-   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsOther));
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<D, FP8>::kOther));
    if (!FP8 && warp == kWarpProducer) {
     // The whole warp walks the schedule (so every operand is warp-uniform); one elected
     // lane issues the TMA copies and the expect-tx arrivals.
@@ -763,7 +783,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
    }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsSoftmax));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<D, FP8>::kSoftmax));
     const int q = warp >> 2;
     const int row = threadIdx.x & 127;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -1038,7 +1058,8 @@ static cudaError_t launch_attn_d(const CascadeParams& p, const CascadeMaps& maps
   if (e != cudaSuccess) return e;
   // the register split must fit in what the block is launched with (else setmaxnreg.inc
   // would wait forever)
-  if (static_cast<int64_t>(attr.numRegs) * kThreads < 256 * C::kRegsSoftmax + 128 * C::kRegsOther)
+  if (static_cast<int64_t>(attr.numRegs) * kThreads <
+      256 * Regs<D, FP8>::kSoftmax + 128 * Regs<D, FP8>::kOther)
     return cudaErrorInvalidConfiguration;
   e = cudaFuncSetAttribute(cascade_attn_kernel<D, FP8>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
