@@ -66,6 +66,7 @@ constexpr int kThreads = 384;             // three warpgroups
 // holds; the host checks the compiled register count before launching.
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
+constexpr int kWarpFillCheck = 10;  // BF16 variant (the FP8 variant uses warp 10 to load)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: O is rescaled only past 2^8
 constexpr int kSortBins = 1024;
 constexpr uint32_t kTmemCols = 512;
@@ -436,7 +437,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       mbar_init(&bars->q_full[q], 1);
       mbar_init(&bars->q_empty[q], 1);
       mbar_init(&bars->s_full[q], 1);
-      mbar_init(&bars->p_full[q], 4);  // one arrival per softmax warp
+      // one arrival per softmax warp (+ the fill checker in the BF16 variant)
+      mbar_init(&bars->p_full[q], FP8 ? 4 : 5);
       mbar_init(&bars->o_done[q], 1);
     }
     for (int s = 0; s < C::kStages; ++s) {
@@ -664,6 +666,42 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       }
       it = nxt;
     }
+   } else if (!FP8 && warp == kWarpFillCheck) {
+    // ------------------------------------------------ BF16 variant: fill checker
+    // For every group {PV(q,k), S(q,k+1)}: wait until the V(q,k) and K(q,k+1) fills it
+    // reads have landed, then add the fifth arrival on p_full[q]. Before arriving for a
+    // group it waits for the previous phase of p_full[q] to complete, so it never gives
+    // two arrivals to one phase.
+    uint32_t kv_base = 0, arrived[2] = {0, 0};
+    bool ok = true;
+    int item = blockIdx.x;
+    Item it = item < total_items ? load_item(p, item) : Item{};
+    for (; ok && item < total_items; item += stride) {
+      const Item nxt = item + stride < total_items ? load_item(p, item + stride) : it;
+      const int nA = it.n_anchor_tiles();
+      const int nS = it.n_sfx_tiles();
+      const int n = nA + nS;
+      for (int k = 0; ok && k < n; ++k) {
+        for (int q = 0; ok && q < 2; ++q) {
+          if (k >= nA || q == 0) {
+            const uint32_t seq = kv_base + pos_of(nA, q, k);
+            ok = wait_parity_warp(wc, &bars->v_full[seq % C::kStages], (seq / C::kStages) & 1u);
+          }
+          if (ok && k + 1 < n && (k + 1 >= nA || q == 0)) {
+            const uint32_t seq = kv_base + pos_of(nA, q, k + 1);
+            ok = wait_parity_warp(wc, &bars->k_full[seq % C::kStages], (seq / C::kStages) & 1u);
+          }
+          if (ok && arrived[q] > 0)
+            ok = wait_parity_warp(wc, &bars->p_full[q], (arrived[q] - 1) & 1u);
+          if (!ok) break;
+          ++arrived[q];
+          if (lane == 0) mbar_arrive(&bars->p_full[q]);
+          __syncwarp();
+        }
+      }
+      kv_base += nA + 2 * nS;
+      it = nxt;
+    }
    } else if (warp == kWarpMma) {
     // Whole warp walks the schedule; one elected lane issues tcgen05.mma / commit.
     {
@@ -691,7 +729,11 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
 
         // Waits (K fill, Q fill) for S(q, k) and (V fill, P ready) for PV(q, k); the MMAs
         // are issued only after every wait of the next pair of groups is done, so PV(q, k)
-        // and S(q, k + 1) go to the tensor pipe back to back.
+        // and S(q, k + 1) go to the tensor pipe back to back. In the BF16 variant the fill
+        // checker warp folds the V(q,k) and K(q,k+1) fills into p_full[q], so after the
+        // first group of an item the MMA warp waits once per group: an mbarrier wait costs
+        // it a few hundred cycles while the tensor pipe reads shared memory, and the pipe's
+        // queue holds only about two MMAs.
         auto wait_s = [&](int q, int k) -> bool {
           const uint32_t seq = kv_base + pos_of(nA, q, k);
           const int slot = seq % C::kStages;
@@ -706,7 +748,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           const int slot = seq % C::kStages;
           const uint32_t ph = (seq / C::kStages) & 1u;
           const bool sfx = k >= nA;
-          if ((sfx || q == 0) && !wait_parity_warp(wc, &bars->v_full[slot], ph)) return false;
+          if (FP8 && (sfx || q == 0) && !wait_parity_warp(wc, &bars->v_full[slot], ph))
+            return false;
           if (!wait_parity_warp(wc, &bars->p_full[q], p_cnt[q] & 1u)) return false;
           ++p_cnt[q];
           return true;
@@ -762,7 +805,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         }
         for (int k = 0; ok && k < n; ++k) {
           for (int q = 0; q < 2 && ok; ++q) {
-            ok = wait_pv(q, k) && (k + 1 >= n || wait_s(q, k + 1));
+            // BF16: the fill checker's arrival on p_full covers V(q,k) and K(q,k+1)
+            ok = wait_pv(q, k) && (!FP8 || k + 1 >= n || wait_s(q, k + 1));
             if (!ok) break;
             tc_fence_after();
             if (leader) {

@@ -52,6 +52,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test: has the phase with parity `parity` completed?
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // State shared by the roles of one CTA for bounded waits.
 struct WaitCtl {
   uint64_t timeout_ns;       // how long one wait may block
@@ -62,8 +75,7 @@ struct WaitCtl {
 // Waits until the phase with parity `parity` of `bar` has completed. Returns false (and
 // raises the CTA's abort flag) if the wait blocks longer than the limit or another role
 // of the CTA aborted first.
-__device__ __forceinline__ bool wait_parity(const WaitCtl& w, uint64_t* bar, uint32_t parity) {
-  const uint32_t a = smem_u32(bar);
+__device__ __forceinline__ bool wait_parity_at(const WaitCtl& w, uint32_t a, uint32_t parity) {
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t deadline = global_timer_ns() + w.timeout_ns;
   for (uint32_t i = 1;; ++i) {
@@ -77,6 +89,9 @@ __device__ __forceinline__ bool wait_parity(const WaitCtl& w, uint64_t* bar, uin
       }
     }
   }
+}
+__device__ __forceinline__ bool wait_parity(const WaitCtl& w, uint64_t* bar, uint32_t parity) {
+  return wait_parity_at(w, smem_u32(bar), parity);
 }
 
 // One lane of a converged warp (the same lane every time the warp is converged).
