@@ -263,6 +263,9 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
   p.order = reinterpret_cast<int32_t*>(wsb + wl.order);
   p.seg = reinterpret_cast<int32_t*>(wsb + wl.seg);
   p.items = reinterpret_cast<int32_t*>(wsb + wl.items);
+  p.redo_count = reinterpret_cast<int32_t*>(wsb + wl.redo_count);
+  p.redo_flag = reinterpret_cast<int32_t*>(wsb + wl.redo_flag);
+  p.redo_list = reinterpret_cast<int32_t*>(wsb + wl.redo_list);
   p.err_word = st->err_word;
   {
     std::lock_guard<std::mutex> lock(g_mutex);

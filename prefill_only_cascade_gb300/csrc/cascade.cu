@@ -68,6 +68,16 @@ constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 constexpr int kWarpFillCheck = 10;  // BF16 variant (the FP8 variant uses warp 10 to load)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: O is rescaled only past 2^8
+// Fast kernel: P = 2^(s c) with no max subtracted is used as long as every valid row's
+// max of s c (log2 units) lies in [-kSpecLow, kSpecHigh]; else the item goes to the exact
+// kernel. bf16 P: up to 2^32 keeps O and l far from fp32 overflow, down to 2^-64 far from
+// underflow. f16 P (FP8 variant, times v_scale) must stay below 65504 and its largest
+// value above the f16 normal range, hence [2^-8, 2^8].
+template <bool F16P>
+struct SpecBounds {
+  static constexpr float kHigh = F16P ? 8.0f : 32.0f;
+  static constexpr float kLow = F16P ? 8.0f : 64.0f;
+};
 constexpr int kSortBins = 1024;
 constexpr uint32_t kTmemCols = 512;
 
@@ -322,20 +332,27 @@ __device__ __forceinline__ void store_e4m3_regs(uint32_t tile, const uint4 (&v)[
 }
 
 // ---------------------------------------------------------------------------------
-// Softmax of one S tile of NC columns: mask, row max, lazy rescale of O, P = 2^(s c - m)
-// written back to TMEM as bf16 (f16 times pscale in the FP8 variant) over columns
-// 0 .. NC/2 of the S region, row sum update.
-template <int NC, int D, bool F16P>
-__device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, bool first_tile,
-                                             bool masked, int lo_c, int hi_c, float c,
-                                             float pscale, float& m_used, float& l) {
+// Softmax of one S tile: one thread per row, NC columns; P = 2^(s c - m) is written back
+// to TMEM (bf16 pairs; f16 times pscale in the FP8 variant, pscale = v_scale on anchor
+// tiles) over the upper half of the S columns, and l accumulates the unscaled P.
+//
+// Two kernels share this code:
+//  * the fast kernel uses m = 0 throughout: no max pass and no rescale of O. The row max
+//    is computed alongside the exponentials, and an item with a valid row whose max falls
+//    outside SpecBounds (P could overflow, or all of it underflow) is listed for the
+//    exact kernel, which writes its output rows again;
+//  * the exact kernel recomputes those items with the usual online softmax (lazy rescale
+//    of O past 2^kRescaleThreshold).
+
+template <int NC>
+__device__ __forceinline__ void load_s(uint32_t t_s, bool masked, int lo_c, int hi_c,
+                                       float (&s)[NC]) {
   uint32_t r[NC / 32][32];
 #pragma unroll
   for (int ch = 0; ch < NC / 32; ++ch) tmem_ld32(t_s + ch * 32, r[ch]);
   tmem_wait_ld_dep(r[0]);
 #pragma unroll
   for (int ch = 1; ch < NC / 32; ++ch) reg_dep(r[ch]);
-  float s[NC];
 #pragma unroll
   for (int j = 0; j < NC; ++j) s[j] = __uint_as_float(r[j / 32][j % 32]);
   if (masked) {
@@ -343,7 +360,49 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, bool fi
     for (int j = 0; j < NC; ++j)
       if (j < lo_c || j > hi_c) s[j] = -INFINITY;
   }
-  // row max: 8 independent chains of 3-input maxes, then a small tree
+}
+
+// P = 2^(s c - m_safe) for all NC columns, packed in pairs and stored to TMEM at t_p
+// 32 columns (16 packed) at a time as they are made; returns the row sum of P and, if
+// WITH_MAX, the row max of s (8 independent chains of 3-input maxes, off the exp path).
+template <int NC, bool F16P, bool WITH_MAX>
+__device__ __forceinline__ float exp_store(const float (&s)[NC], float c, float m_safe,
+                                           float pscale, uint32_t t_p, float& mx) {
+  const uint64_t cc = f2(c, c);
+  const uint64_t nm = f2(-m_safe, -m_safe);
+  uint64_t acc[4] = {0, 0, 0, 0};  // four packed partial sums (+0.0f bit patterns)
+  float m8[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
+#pragma unroll
+  for (int ch = 0; ch < NC / 32; ++ch) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int e = ch * 32 + 2 * j;
+      if (WITH_MAX && (j % 8) == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m8[i] = max3(m8[i], s[e + i], s[e + 8 + i]);
+      }
+      const uint64_t x = f2_fma(f2(s[e], s[e + 1]), cc, nm);
+      float x0, x1;
+      f2_split(x, x0, x1);
+      const float p0 = ex2(x0), p1 = ex2(x1);
+      acc[j & 3] = f2_add(acc[j & 3], f2(p0, p1));
+      pk[j] = F16P ? pack_p<true>(p0 * pscale, p1 * pscale) : pack_p<false>(p0, p1);
+    }
+    tmem_st16(t_p + ch * 16, pk);
+  }
+  if (WITH_MAX)
+    mx = fmaxf(max3(m8[0], m8[1], m8[2]), fmaxf(max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+  const uint64_t acc2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+  float sa, sb;
+  f2_split(acc2, sa, sb);
+  return sa + sb;
+}
+
+template <int NC>
+__device__ __forceinline__ float row_max(const float (&s)[NC]) {
   float m8[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) m8[i] = s[i];
@@ -355,9 +414,17 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, bool fi
 #pragma unroll
     for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[NC - 8 + i]);
   }
-  const float mx = fmaxf(max3(m8[0], m8[1], m8[2]),
-                         fmaxf(max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-  const float m_tile = mx * c;
+  return fmaxf(max3(m8[0], m8[1], m8[2]), fmaxf(max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+}
+
+// Exact online softmax (the recompute kernel).
+template <int NC, int D, bool F16P>
+__device__ __forceinline__ void softmax_tile_exact(uint32_t t_s, uint32_t t_o, bool first_tile,
+                                                   bool masked, int lo_c, int hi_c, float c,
+                                                   float pscale, float& m_used, float& l) {
+  float s[NC];
+  load_s<NC>(t_s, masked, lo_c, hi_c, s);
+  const float m_tile = row_max<NC>(s) * c;
   float alpha = 1.0f;
   bool rescale = false;
   if (first_tile) {
@@ -368,31 +435,9 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, bool fi
     rescale = true;
   }
   const float m_safe = (m_used == -INFINITY) ? 0.0f : m_used;
-  const uint64_t cc = f2(c, c);
-  const uint64_t nm = f2(-m_safe, -m_safe);
-  uint64_t acc[4] = {0, 0, 0, 0};  // four packed partial sums (+0.0f bit patterns)
-#pragma unroll
-  for (int ch = 0; ch < NC / 32; ++ch) {
-    uint32_t pk[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const uint64_t x = f2_fma(f2(s[ch * 32 + 2 * j], s[ch * 32 + 2 * j + 1]), cc, nm);
-      float x0, x1;
-      f2_split(x, x0, x1);
-      const float p0 = ex2(x0), p1 = ex2(x1);
-      acc[j & 3] = f2_add(acc[j & 3], f2(p0, p1));
-      if (F16P) {
-        pk[j] = pack_p<true>(p0 * pscale, p1 * pscale);  // anchor tiles: P * v_scale
-      } else {
-        pk[j] = pack_p<false>(p0, p1);
-      }
-    }
-    tmem_st16(t_s + ch * 16, pk);
-  }
-  const uint64_t acc2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
-  float sa, sb;
-  f2_split(acc2, sa, sb);
-  l = l * alpha + (sa + sb);
+  float unused;
+  const float sum = exp_store<NC, F16P, false>(s, c, m_safe, pscale, t_s + NC / 2, unused);
+  l = l * alpha + sum;
   // The PV of the previous tile is complete (the commit that signalled this S tile
   // tracks every earlier MMA), and the PV of this tile waits for this warpgroup's P,
   // so O can be rescaled in place here.
@@ -416,12 +461,31 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, bool fi
   tmem_wait_st();
 }
 
+// Fast kernel: P = 2^(s c) against the fixed reference m = 0 (no max pass, no rescale).
+// Returns the tile's row max of s c (computed alongside the exponentials).
+template <int NC, bool F16P>
+__device__ __forceinline__ float softmax_tile_spec(uint32_t t_s, bool masked, int lo_c, int hi_c,
+                                                   float c, float pscale, float& l) {
+  float s[NC];
+  load_s<NC>(t_s, masked, lo_c, hi_c, s);
+  float mx;
+  l += exp_store<NC, F16P, true>(s, c, 0.0f, pscale, t_s + NC / 2, mx);
+  tmem_wait_st();
+  return mx * c;
+}
+
 // ---------------------------------------------------------------------------------
-template <int D, bool FP8>
+// EXACT = false: the fast kernel over all work items. EXACT = true: the exact kernel over
+// the items the fast kernel listed in redo_list (its CTAs return at once if none).
+template <int D, bool FP8, bool EXACT>
 __global__ void __launch_bounds__(kThreads, 1)
 cascade_attn_kernel(const __grid_constant__ CascadeParams p,
                     const __grid_constant__ CascadeMaps maps) {
   using C = Cfg<D>;
+  // work items this kernel walks; position i of the walk is item item_id(i)
+  const int total_items = EXACT ? *p.redo_count : __ldg(p.prefix + p.num_anchors);
+  if (EXACT && static_cast<int>(blockIdx.x) >= total_items) return;
+  auto item_id = [&](int i) { return EXACT ? __ldg(p.redo_list + i) : i; };
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -466,7 +530,6 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
   wc.abort_flag = &bars->abort_flag;
   wc.err_word = p.err_word;
 
-  const int total_items = __ldg(p.prefix + p.num_anchors);
   const int tok = p.tok_per_tile;
   const int G = p.group;
   const int hkv = p.hkv;
@@ -493,9 +556,9 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       bool skip_pending = p.inject_skip_first_kv != 0;
       bool ok = true;
       int item = blockIdx.x;
-      Item it = item < total_items ? load_item(p, item) : Item{};
+      Item it = item < total_items ? load_item(p, item_id(item)) : Item{};
       for (; ok && item < total_items; item += stride, ++it_count) {
-        const Item nxt = item + stride < total_items ? load_item(p, item + stride) : it;
+        const Item nxt = item + stride < total_items ? load_item(p, item_id(item + stride)) : it;
         const int nA = it.n_anchor_tiles();
         const int n_tiles = nA + 2 * it.n_sfx_tiles();
         const int g = it.ag % hkv;
@@ -594,9 +657,9 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
     uint32_t kv_seq = 0, it_count = 0;
     bool ok = true;
     int item = blockIdx.x;
-    Item it = item < total_items ? load_item(p, item) : Item{};
+    Item it = item < total_items ? load_item(p, item_id(item)) : Item{};
     for (; ok && item < total_items; item += stride, ++it_count) {
-      const Item nxt = item + stride < total_items ? load_item(p, item + stride) : it;
+      const Item nxt = item + stride < total_items ? load_item(p, item_id(item + stride)) : it;
       const int nA = it.n_anchor_tiles();
       const int n_tiles = nA + 2 * it.n_sfx_tiles();
       const int nk_sfx = it.nk_sfx();
@@ -675,9 +738,9 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
     uint32_t kv_base = 0, arrived[2] = {0, 0};
     bool ok = true;
     int item = blockIdx.x;
-    Item it = item < total_items ? load_item(p, item) : Item{};
+    Item it = item < total_items ? load_item(p, item_id(item)) : Item{};
     for (; ok && item < total_items; item += stride) {
-      const Item nxt = item + stride < total_items ? load_item(p, item + stride) : it;
+      const Item nxt = item + stride < total_items ? load_item(p, item_id(item + stride)) : it;
       const int nA = it.n_anchor_tiles();
       const int nS = it.n_sfx_tiles();
       const int n = nA + nS;
@@ -719,9 +782,9 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       uint32_t p_cnt[2] = {0, 0};
       bool ok = true;
       int item = blockIdx.x;
-      Item it = item < total_items ? load_item(p, item) : Item{};
+      Item it = item < total_items ? load_item(p, item_id(item)) : Item{};
       for (; ok && item < total_items; item += stride, ++it_count) {
-        const Item nxt = item + stride < total_items ? load_item(p, item + stride) : it;
+        const Item nxt = item + stride < total_items ? load_item(p, item_id(item + stride)) : it;
         const int nA = it.n_anchor_tiles();
         const int nS = it.n_sfx_tiles();
         const int nk_sfx = it.nk_sfx();
@@ -779,7 +842,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           const bool sfx = k >= nA;
           const uint32_t v_lo = v_lo0 + slot * (2 * C::kTileBytes >> 4);
           const uint32_t d_o = tmem + 256u * q + 128u;
-          const uint32_t a_p = tmem + 256u * q;
+          // P sits over the upper half of the S columns (64 of 128, or 32 of 64)
+          const uint32_t a_p = tmem + 256u * q + ((sfx && nk_sfx == 64) ? 32u : 64u);
           const uint32_t acc0 = k > 0 ? 1u : 0u;
           // 16 keys per step: 16 rows of 128 bytes of V; P columns advance by 8 (2 x bf16)
 #pragma unroll
@@ -794,14 +858,15 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           if (k == n - 1) mma_commit(&bars->o_done[q]);
         };
 
-        ok = wait_s(0, 0) && wait_s(1, 0);
-        if (ok) {
-          tc_fence_after();
-          if (leader) {
-            mma_s(0, 0);
-            mma_s(1, 0);
+        // S(0,0) goes as soon as its own K and Q fills are in (the Q fills of an item land
+        // one after the other).
+        for (int q = 0; q < 2 && ok; ++q) {
+          ok = wait_s(q, 0);
+          if (ok) {
+            tc_fence_after();
+            if (leader) mma_s(q, 0);
+            __syncwarp();
           }
-          __syncwarp();
         }
         for (int k = 0; ok && k < n; ++k) {
           for (int q = 0; q < 2 && ok; ++q) {
@@ -837,9 +902,9 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
     bool ok = true;
     const float c = p.scale_log2;
     int item = blockIdx.x;
-    Item it = item < total_items ? load_item(p, item) : Item{};
+    Item it = item < total_items ? load_item(p, item_id(item)) : Item{};
     for (; ok && item < total_items; item += stride, ++it_count) {
-      const Item nxt = item + stride < total_items ? load_item(p, item + stride) : it;
+      const Item nxt = item + stride < total_items ? load_item(p, item_id(item + stride)) : it;
       const int nA = it.n_anchor_tiles();
       const int n = nA + it.n_sfx_tiles();
       const int nk_sfx = it.nk_sfx();
@@ -852,28 +917,51 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       // FP8 anchor tiles: scores use c * k_scale, and P carries v_scale
       const float c_anc = FP8 ? c * __ldg(p.k_scale + it.ag) : c;
       const float v_sc = FP8 ? __ldg(p.v_scale + it.ag) : 1.0f;
-      float m_used = -INFINITY, l = 0.0f;
+      float m_used = EXACT ? -INFINITY : 0.0f, l = 0.0f;
+      float row_mx = -INFINITY;  // fast kernel: max of s c over the row's tiles
       for (int k = 0; k < n; ++k) {
         if (!(ok = wait_parity(wc, &bars->s_full[q], s_cnt & 1u))) break;
         ++s_cnt;
         tc_fence_after();
         if (k < nA) {
           const int rem = it.la - k * kBN;
-          softmax_tile<128, D, FP8>(t_s, t_o, k == 0, rem < kBN, 0, rem - 1, c_anc, v_sc,
-                                    m_used, l);
+          if (EXACT)
+            softmax_tile_exact<128, D, FP8>(t_s, t_o, k == 0, rem < kBN, 0, rem - 1, c_anc,
+                                            v_sc, m_used, l);
+          else
+            row_mx = fmaxf(row_mx, softmax_tile_spec<128, FP8>(t_s, rem < kBN, 0, rem - 1,
+                                                               c_anc, v_sc, l));
         } else {
           const int base = ws_q + (k - nA) * kBN;
           const int lo_c = vis_lo - base, hi_c = t - base;
-          if (nk_sfx == 64)
-            softmax_tile<64, D, FP8>(t_s, t_o, k == 0, true, lo_c, hi_c, c, 1.0f, m_used, l);
-          else
-            softmax_tile<128, D, FP8>(t_s, t_o, k == 0, true, lo_c, hi_c, c, 1.0f, m_used, l);
+          if (EXACT) {
+            if (nk_sfx == 64)
+              softmax_tile_exact<64, D, FP8>(t_s, t_o, k == 0, true, lo_c, hi_c, c, 1.0f,
+                                             m_used, l);
+            else
+              softmax_tile_exact<128, D, FP8>(t_s, t_o, k == 0, true, lo_c, hi_c, c, 1.0f,
+                                              m_used, l);
+          } else {
+            if (nk_sfx == 64)
+              row_mx = fmaxf(row_mx, softmax_tile_spec<64, FP8>(t_s, true, lo_c, hi_c, c,
+                                                                1.0f, l));
+            else
+              row_mx = fmaxf(row_mx, softmax_tile_spec<128, FP8>(t_s, true, lo_c, hi_c, c,
+                                                                 1.0f, l));
+          }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full[q]);
       }
       if (!ok) break;
+      // Fast kernel: hand the item to the exact kernel if a valid row left the bounds
+      // (its output rows are then written again).
+      const bool broke = !(row_mx >= -SpecBounds<FP8>::kLow && row_mx <= SpecBounds<FP8>::kHigh);
+      if (!EXACT && __any_sync(0xFFFFFFFFu, broke && valid) && lane == 0) {
+        const int id = item_id(item);
+        if (atomicExch(p.redo_flag + id, 1) == 0) p.redo_list[atomicAdd(p.redo_count, 1)] = id;
+      }
       if (!(ok = wait_parity(wc, &bars->o_done[q], it_count & 1u))) break;
       tc_fence_after();
       const float inv_l = 1.0f / l;
@@ -980,7 +1068,10 @@ __global__ void __launch_bounds__(1024) cascade_schedule_kernel(const CascadePar
   int32_t* prefix = p.prefix;
   int32_t* order = p.order;
   const int tid = threadIdx.x;
-  if (tid == 0) bad = 0;
+  if (tid == 0) {
+    bad = 0;
+    *p.redo_count = 0;
+  }
   for (int i = tid; i < kSortBins; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   int my_bad = 0;
@@ -1043,6 +1134,7 @@ __global__ void __launch_bounds__(256) cascade_items_kernel(const CascadeParams 
   const int A = p.num_anchors;
   const int total = p.prefix[A];
   if (item >= total) return;
+  p.redo_flag[item] = 0;
   int lo = 0, hi = A - 1;  // largest sorted position with prefix <= item
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -1085,33 +1177,46 @@ CascadeWorkspace cascade_workspace_layout(int num_anchors, int64_t total_suffix_
   auto up = [](size_t x, size_t a) { return (x + a - 1) / a * a; };
   CascadeWorkspace w;
   w.flag = 0;
+  w.redo_count = 4;
   w.prefix = 16;
   w.order = w.prefix + 4 * (static_cast<size_t>(num_anchors) + 1);
   w.seg = up(w.order + 4 * static_cast<size_t>(num_anchors), 16);
   w.items = up(w.seg + 4 * static_cast<size_t>(total_suffix_tokens), 32);
-  w.total = up(w.items + 32 * static_cast<size_t>(item_bound), 256);
+  w.redo_flag = w.items + 32 * static_cast<size_t>(item_bound);
+  w.redo_list = w.redo_flag + 4 * static_cast<size_t>(item_bound);
+  w.total = up(w.redo_list + 4 * static_cast<size_t>(item_bound), 256);
   return w;
 }
 
-template <int D, bool FP8>
-static cudaError_t launch_attn_d(const CascadeParams& p, const CascadeMaps& maps, int num_sms,
-                                 cudaStream_t stream) {
+template <int D, bool FP8, bool EXACT>
+static cudaError_t launch_attn_kernel(const CascadeParams& p, const CascadeMaps& maps,
+                                      int num_sms, cudaStream_t stream) {
   using C = Cfg<D>;
   cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, cascade_attn_kernel<D, FP8>);
+  cudaError_t e = cudaFuncGetAttributes(&attr, cascade_attn_kernel<D, FP8, EXACT>);
   if (e != cudaSuccess) return e;
   // the register split must fit in what the block is launched with (else setmaxnreg.inc
   // would wait forever)
   if (static_cast<int64_t>(attr.numRegs) * kThreads <
       256 * Regs<D, FP8>::kSoftmax + 128 * Regs<D, FP8>::kOther)
     return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(cascade_attn_kernel<D, FP8>,
+  e = cudaFuncSetAttribute(cascade_attn_kernel<D, FP8, EXACT>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = p.item_bound < num_sms ? p.item_bound : num_sms;
   if (grid <= 0) return cudaSuccess;
-  cascade_attn_kernel<D, FP8><<<grid, kThreads, C::kSmemBytes, stream>>>(p, maps);
+  cascade_attn_kernel<D, FP8, EXACT><<<grid, kThreads, C::kSmemBytes, stream>>>(p, maps);
   return cudaGetLastError();
+}
+
+// The fast kernel, then the exact kernel over the items it handed over (none: its CTAs
+// return at once).
+template <int D, bool FP8>
+static cudaError_t launch_attn_d(const CascadeParams& p, const CascadeMaps& maps, int num_sms,
+                                 cudaStream_t stream) {
+  cudaError_t e = launch_attn_kernel<D, FP8, false>(p, maps, num_sms, stream);
+  if (e != cudaSuccess) return e;
+  return launch_attn_kernel<D, FP8, true>(p, maps, num_sms, stream);
 }
 
 cudaError_t launch_cascade(const CascadeParams& p, const CascadeMaps& maps, int head_dim,

@@ -62,6 +62,9 @@ struct CascadeParams {
   int32_t* order;            // [A] anchors by decreasing anchor-tile count
   int32_t* seg;              // [T_S] first token of the suffix that holds each token
   int32_t* items;            // [item_bound][8] one record per work item
+  int32_t* redo_count;       // items the speculative kernel handed to the exact one
+  int32_t* redo_flag;        // [item_bound] nonzero: item is in redo_list
+  int32_t* redo_list;        // [item_bound] item indices, redo_count of them valid
   unsigned* err_word;
   uint64_t timeout_ns;
   int inject_skip_first_kv;
@@ -69,7 +72,7 @@ struct CascadeParams {
 
 // Byte offsets of the workspace regions; `total` is the size to allocate.
 struct CascadeWorkspace {
-  size_t flag, prefix, order, seg, items, total;
+  size_t flag, redo_count, prefix, order, seg, items, redo_flag, redo_list, total;
 };
 CascadeWorkspace cascade_workspace_layout(int num_anchors, int64_t total_suffix_tokens,
                                           int64_t item_bound);

@@ -26,8 +26,10 @@ def layout_tensors(layout, device="cuda"):
 
 
 def run_cascade(cfg_heads, layout, t, kv_fp8=False, k_scale=None, v_scale=None,
-                softmax_scale=0.0, with_lse=True):
-    """Call quail_cascade_attn on device tensors `t` (keys as in workloads)."""
+                softmax_scale=0.0, with_lse=True, keep_ws=False):
+    """Call quail_cascade_attn on device tensors `t` (keys as in workloads). With keep_ws
+    the workspace is returned too (its int32 at byte 4 counts the work items the fast
+    kernel handed to the exact one)."""
     import prefill_only_cascade_gb300 as q
     hq, hkv, d = cfg_heads
     dev = t["q_suf"].device
@@ -45,7 +47,14 @@ def run_cascade(cfg_heads, layout, t, kv_fp8=False, k_scale=None, v_scale=None,
     torch.cuda.synchronize()
     st = q.get_device_error()
     assert st == q.QUAIL_OK, q.status_string(st)
+    if keep_ws:
+        return out, lse, ws
     return out, lse
+
+
+def redo_count(ws):
+    """Work items the fast kernel listed for the exact kernel in the last call."""
+    return int(ws[4:8].view(torch.int32).item())
 
 
 def np64(x):

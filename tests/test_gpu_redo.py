@@ -1,0 +1,99 @@
+"""GPU parity of the exact recompute path.
+
+The fast cascade kernel computes P = 2^(s c) with no max subtracted and lists a work item
+for the exact kernel when a valid row's max of s c leaves its bounds (bf16 P: [-64, 32],
+FP8 variant: [-8, 8], log2 units). Seeded inputs with large or very negative logits force
+that path, for all items or only some; every output element is compared with the float64
+oracle, and the workspace's redo counter shows the exact kernel did run."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from oracle.fp8 import dequantize_kv_fp8
+from parity_util import FP8_REL_L2, check_full, np64, redo_count, run_cascade
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(anchors, counts, lens, heads, seed):
+    rng = np.random.default_rng(seed)
+    if isinstance(lens, tuple):
+        lens = rng.integers(lens[0], lens[1] + 1, size=sum(counts))
+    lay = workloads.layout_from_lengths(anchors, counts, lens)
+    hq, hkv, d = heads
+    cfg = workloads.AttnConfig("redo", lay.num_anchors, (0, 0), 0, (0, 0), hq, hkv, d, False,
+                               seed)
+    return lay, workloads.make_attention_inputs(cfg, lay, "cuda")
+
+
+def test_normal_inputs_need_no_recompute():
+    lay, t = _case([300, 40], [4, 3], (1, 40), (8, 2, 128), 3)
+    out, lse, ws = run_cascade((8, 2, 128), lay, t, keep_ws=True)
+    assert redo_count(ws) == 0
+    check_full((8, 2, 128), lay, t, out, lse)
+
+
+@pytest.mark.parametrize("heads", [(8, 2, 128), (16, 1, 64)])
+def test_large_logits_every_item_recomputed(heads):
+    # queries x 24: s c has a spread of ~35 (log2 units), above the bf16 bound of 32
+    lay, t = _case([300, 0, 129], [4, 2, 3], (1, 40), heads, 11)
+    t["q_suf"] = (t["q_suf"].float() * 24).to(torch.bfloat16)
+    out, lse, ws = run_cascade(heads, lay, t, keep_ws=True)
+    assert redo_count(ws) > 0
+    check_full(heads, lay, t, out, lse)
+
+
+def test_one_anchor_recomputed_others_fast():
+    lay, t = _case([200, 300, 150], [3, 3, 3], (2, 30), (8, 2, 128), 12)
+    ao = lay.anchor_offsets
+    # anchor 1's keys x 40: only its items leave the bounds
+    t["k_anc"][int(ao[1]):int(ao[2])] = (t["k_anc"][int(ao[1]):int(ao[2])].float() * 40).to(
+        torch.bfloat16)
+    out, lse, ws = run_cascade((8, 2, 128), lay, t, keep_ws=True)
+    # exactly anchor 1's items: 2 KV heads x ceil(tokens / 64) query-tile pairs (G = 4)
+    so, asp = lay.suffix_offsets, lay.anchor_suffix_ptr
+    ntok = int(so[asp[2]] - so[asp[1]])
+    assert redo_count(ws) == 2 * ((ntok + 63) // 64)
+    check_full((8, 2, 128), lay, t, out, lse)
+
+
+def test_very_negative_scores_recomputed():
+    # every key equal to v (|v| = 32), queries = -0.75 v: all scores equal,
+    # s c = -0.75 * 1024 * log2(e) / sqrt(128) ~ -98, below the bf16 lower bound of -64
+    lay, t = _case([256], [4], (1, 20), (8, 2, 128), 13)
+    g = torch.Generator(device="cpu").manual_seed(13)
+    v = torch.randn(128, generator=g)
+    v = (v / v.norm() * 32).to(torch.bfloat16).to("cuda")
+    for name in ("k_anc", "k_suf"):
+        t[name][:] = v
+    t["q_suf"][:] = (-v.float() * 0.75).to(torch.bfloat16)
+    out, lse, ws = run_cascade((8, 2, 128), lay, t, keep_ws=True)
+    assert redo_count(ws) > 0
+    check_full((8, 2, 128), lay, t, out, lse)
+
+
+def test_fp8_large_logits_recomputed():
+    import prefill_only_cascade_gb300 as q
+    lay, t = _case([513, 40], [6, 9], (1, 96), (32, 8, 128), 14)
+    # s c spread ~11 with queries x 8: above the f16-P bound of 8
+    t["q_suf"] = (t["q_suf"].float() * 8).to(torch.bfloat16)
+    qz = {}
+    for name in ("k_anc", "v_anc"):
+        codes = torch.empty(t[name].shape, dtype=torch.uint8, device="cuda")
+        scale = torch.empty(lay.num_anchors, 8, dtype=torch.float32, device="cuda")
+        q.quantize_kv_fp8(t[name], t["anchor_offsets"], codes, scale)
+        qz[name] = (codes, scale)
+    t8 = dict(t, k_anc=qz["k_anc"][0], v_anc=qz["v_anc"][0])
+    out, lse, ws = run_cascade((32, 8, 128), lay, t8, kv_fp8=True, k_scale=qz["k_anc"][1],
+                               v_scale=qz["v_anc"][1], keep_ws=True)
+    assert redo_count(ws) > 0
+    kv = []
+    for name in ("k_anc", "v_anc"):
+        codes, scales = oracle.quantize_kv_fp8(np64(t[name]).astype(np.float32),
+                                               lay.anchor_offsets)
+        kv.append(dequantize_kv_fp8(codes, scales, lay.anchor_offsets))
+    check_full((32, 8, 128), lay, t, out, lse, kv=tuple(kv), rel_bound=FP8_REL_L2)
