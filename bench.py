@@ -364,7 +364,8 @@ def run_ours(args):
     roofline = {"bound": "tensor", "achieved": round(achieved_tflops, 2), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved_tflops / peak, 4),
                 "traffic": traffic, "peak_source": f"bf16_tflops (burst) of {src}",
-                "kernel": "cascade_attn_kernel (+ its schedule kernel)",
+                "kernel": "cascade_attn_kernel, fast + exact launches (+ its 3 schedule "
+                          "kernels): one quail_cascade_attn call",
                 "kernel_ms": round(attn_ms, 4),
                 "algorithmic_flops_per_launch": flops,
                 "algorithmic_bytes_per_launch": attention_bytes(
@@ -399,7 +400,8 @@ def run_ours(args):
                    "head_hidden": hcfg.hidden, "head_rows": S,
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": 5 * args.steps, "clocks": clk.summary(),
+        # per step: segments, schedule, items, fast + exact cascade kernels, head
+        "gpu_launches": 6 * args.steps, "clocks": clk.summary(),
     }
     if rank == 0:
         print(json.dumps(line))
