@@ -489,7 +489,7 @@ def run_bandwidth_kernel(args):
         run = lambda: q.quantize_kv_fp8(kv, ao, codes, scale, stream=stream)
         algo_bytes = kv.numel() * 3 + scale.numel() * 4
         units, unit = kv.numel(), "elements/s"
-        kernel = "kv_amax_kernel + kv_quantize_kernel + amax_to_scale_kernel"
+        kernel = "kv_quantize_cluster_kernel"
     for _ in range(max(args.warmup, 3)):
         run()
     torch.cuda.synchronize()

@@ -186,6 +186,26 @@ def test_quantizer_bit_exact_small():
         np.testing.assert_array_equal(codes.cpu().numpy(), ref_codes)
 
 
+@pytest.mark.parametrize("d,anchors", [(128, [4100, 3, 4096]), (64, [8300, 8192, 0])])
+def test_quantizer_long_slices_bit_exact(d, anchors):
+    # a cluster keeps 65,536 16-byte vectors of one (anchor, head) in registers: 4,096 rows
+    # at d = 128, 8,192 at d = 64; longer slices are read twice
+    import prefill_only_cascade_gb300 as q
+    lay = workloads.layout_from_lengths(anchors, [0] * len(anchors), [])
+    g = torch.Generator(device="cuda").manual_seed(5 + d)
+    kv = (torch.randn(lay.total_anchor_tokens, 2, d, generator=g, device="cuda") * 2).to(
+        torch.bfloat16)
+    kv[int(lay.anchor_offsets[1]) - 1, 1, 3] = 300.0   # the max sits in the last row
+    codes = torch.empty(kv.shape, dtype=torch.uint8, device="cuda")
+    scale = torch.empty(len(anchors), 2, dtype=torch.float32, device="cuda")
+    ao = torch.from_numpy(lay.anchor_offsets.copy()).cuda()
+    q.quantize_kv_fp8(kv, ao, codes, scale)
+    torch.cuda.synchronize()
+    ref_codes, ref_scale = oracle.quantize_kv_fp8(np64(kv).astype(np.float32), lay.anchor_offsets)
+    np.testing.assert_array_equal(scale.cpu().numpy(), ref_scale)
+    np.testing.assert_array_equal(codes.cpu().numpy(), ref_codes)
+
+
 def test_quantizer_full_size_scales_and_sampled_codes():
     import prefill_only_cascade_gb300 as q
     cfg = workloads.ATTN_CONFIGS["fp8_long"]
