@@ -68,16 +68,17 @@ constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 constexpr int kWarpFillCheck = 10;  // BF16 variant (the FP8 variant uses warp 10 to load)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: O is rescaled only past 2^8
-// Fast kernel: P = 2^(s c) with no max subtracted is used as long as every valid row's
-// max of s c (log2 units) lies in [-kSpecLow, kSpecHigh]; else the item goes to the exact
-// kernel. bf16 P: up to 2^32 keeps O and l far from fp32 overflow, down to 2^-64 far from
-// underflow. f16 P (FP8 variant, times v_scale) must stay below 65504 and its largest
-// value above the f16 normal range, hence [2^-8, 2^8].
-template <bool F16P>
-struct SpecBounds {
-  static constexpr float kHigh = F16P ? 8.0f : 32.0f;
-  static constexpr float kLow = F16P ? 8.0f : 64.0f;
-};
+// Fast kernel bounds (P = 2^(s c) with no max subtracted); outside them the item goes to
+// the exact kernel.
+//  * bf16 P: the row sum l = sum P must lie in [2^-64, 2^32]. Every P <= l <= 2^32 keeps O
+//    and l far from fp32 overflow (an infinite P makes l infinite, so it is caught), and
+//    l >= 2^-64 keeps the largest P >= 2^-64 / (keys), far inside the bf16/fp32 range.
+//    Testing l needs no row max at all.
+//  * f16 P (FP8 variant, times v_scale): the row max of s c must lie in [-8, 8]: P stays
+//    below 65504 and its largest value is not pushed toward the f16 subnormals.
+constexpr float kSpecSumLow = 5.421010862427522e-20f;   // 2^-64
+constexpr float kSpecSumHigh = 4294967296.0f;            // 2^32
+constexpr float kSpecMaxF16 = 8.0f;
 constexpr int kSortBins = 1024;
 constexpr uint32_t kTmemCols = 512;
 
@@ -337,10 +338,11 @@ __device__ __forceinline__ void store_e4m3_regs(uint32_t tile, const uint4 (&v)[
 // tiles) over the upper half of the S columns, and l accumulates the unscaled P.
 //
 // Two kernels share this code:
-//  * the fast kernel uses m = 0 throughout: no max pass and no rescale of O. The row max
-//    is computed alongside the exponentials, and an item with a valid row whose max falls
-//    outside SpecBounds (P could overflow, or all of it underflow) is listed for the
-//    exact kernel, which writes its output rows again;
+//  * the fast kernel uses m = 0 throughout: no max pass and no rescale of O. An item with
+//    a valid row outside the fast-kernel bounds (P could overflow, or all of it
+//    underflow: tested on l for bf16 P, on the row max - computed alongside the
+//    exponentials - for f16 P) is listed for the exact kernel, which writes its output
+//    rows again;
 //  * the exact kernel recomputes those items with the usual online softmax (lazy rescale
 //    of O past 2^kRescaleThreshold).
 
@@ -462,16 +464,17 @@ __device__ __forceinline__ void softmax_tile_exact(uint32_t t_s, uint32_t t_o, b
 }
 
 // Fast kernel: P = 2^(s c) against the fixed reference m = 0 (no max pass, no rescale).
-// Returns the tile's row max of s c (computed alongside the exponentials).
+// Returns the tile's row max of s c for f16 P (computed alongside the exponentials), -inf
+// for bf16 P (whose bounds are tested on l).
 template <int NC, bool F16P>
 __device__ __forceinline__ float softmax_tile_spec(uint32_t t_s, bool masked, int lo_c, int hi_c,
                                                    float c, float pscale, float& l) {
   float s[NC];
   load_s<NC>(t_s, masked, lo_c, hi_c, s);
-  float mx;
-  l += exp_store<NC, F16P, true>(s, c, 0.0f, pscale, t_s + NC / 2, mx);
+  float mx = -INFINITY;
+  l += exp_store<NC, F16P, F16P>(s, c, 0.0f, pscale, t_s + NC / 2, mx);
   tmem_wait_st();
-  return mx * c;
+  return F16P ? mx * c : -INFINITY;
 }
 
 // ---------------------------------------------------------------------------------
@@ -957,7 +960,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       if (!ok) break;
       // Fast kernel: hand the item to the exact kernel if a valid row left the bounds
       // (its output rows are then written again).
-      const bool broke = !(row_mx >= -SpecBounds<FP8>::kLow && row_mx <= SpecBounds<FP8>::kHigh);
+      const bool broke = FP8 ? !(row_mx >= -kSpecMaxF16 && row_mx <= kSpecMaxF16)
+                             : !(l >= kSpecSumLow && l <= kSpecSumHigh);
       if (!EXACT && __any_sync(0xFFFFFFFFu, broke && valid) && lane == 0) {
         const int id = item_id(item);
         if (atomicExch(p.redo_flag + id, 1) == 0) p.redo_list[atomicAdd(p.redo_count, 1)] = id;
