@@ -127,6 +127,16 @@ struct Item {
   __device__ __forceinline__ int nk_sfx() const {
     return (n_sfx_tiles() == 1 && window() <= 64) ? 64 : 128;
   }
+  // Both query tiles' suffix windows start at the same token (both inside one suffix, or
+  // q1 inside the suffix where q0 ends): then the BF16 variant lets them share their
+  // suffix tiles as they share the anchor tiles (q0 masks the keys past its rows). The FP8
+  // variant keeps them separate (measured faster there).
+  template <bool FP8>
+  __device__ __forceinline__ bool sfx_shared() const { return !FP8 && ws0 == ws1; }
+  template <bool FP8>
+  __device__ __forceinline__ int n_tiles() const {
+    return n_anchor_tiles() + (sfx_shared<FP8>() ? 1 : 2) * n_sfx_tiles();
+  }
 };
 
 __device__ __forceinline__ int4 ld_nc_v4(const int32_t* p) {
@@ -146,10 +156,10 @@ __device__ __forceinline__ Item load_item(const CascadeParams& p, int item) {
   return it;
 }
 
-// Ring position -> what it holds: anchor tile k (k < nA) or the suffix tile i of query
-// tile q at position nA + 2i + q.
-__device__ __forceinline__ int pos_of(int nA, int q, int k) {
-  return k < nA ? k : nA + 2 * (k - nA) + q;
+// Ring position -> what it holds: anchor tile k (k < nA), then the suffix tiles: shared,
+// suffix tile i at position nA + i; else suffix tile i of query tile q at nA + 2i + q.
+__device__ __forceinline__ int pos_of(int nA, bool shared, int q, int k) {
+  return (k < nA || shared) ? k : nA + 2 * (k - nA) + q;
 }
 
 __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity, uint64_t deadline) {
@@ -563,7 +573,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       for (; ok && item < total_items; item += stride, ++it_count) {
         const Item nxt = item + stride < total_items ? load_item(p, item_id(item + stride)) : it;
         const int nA = it.n_anchor_tiles();
-        const int n_tiles = nA + 2 * it.n_sfx_tiles();
+        const int n_tiles = it.template n_tiles<FP8>();
+        const bool sh = it.template sfx_shared<FP8>();
         const int g = it.ag % hkv;
         for (int pos = 0; pos < n_tiles; ++pos, ++kv_seq) {
           const int slot = kv_seq % C::kStages;
@@ -581,7 +592,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
             const int rel = pos - nA;
             mk = &maps.k_suf;
             mv = &maps.v_suf;
-            row = it.ws(rel & 1) + (rel >> 1) * kBN;
+            row = sh ? it.ws0 + rel * kBN : it.ws(rel & 1) + (rel >> 1) * kBN;
             pol = stream_pol;
           }
           uint8_t* k_dst = sKV + slot * 2 * C::kTileBytes;
@@ -664,7 +675,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
     for (; ok && item < total_items; item += stride, ++it_count) {
       const Item nxt = item + stride < total_items ? load_item(p, item_id(item + stride)) : it;
       const int nA = it.n_anchor_tiles();
-      const int n_tiles = nA + 2 * it.n_sfx_tiles();
+      const int n_tiles = it.template n_tiles<FP8>();
+      const bool sh = it.template sfx_shared<FP8>();
       const int nk_sfx = it.nk_sfx();
       const int g = it.ag % hkv;
       for (int q = 0; q < 2; ++q) {
@@ -711,7 +723,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           publish(&bars->v_full[slot]);
         } else {
           const int rel = pos - nA;
-          const int64_t tok0 = it.ws(rel & 1) + (rel >> 1) * kBN;
+          const int64_t tok0 = sh ? it.ws0 + rel * kBN : it.ws(rel & 1) + (rel >> 1) * kBN;
           const int valid = clamp_rows(T_S - tok0, nk_sfx);
           for (int w = 0; w < 2 && ok; ++w) {  // w = 0: K, w = 1: V
             uint64_t* empty = w ? &bars->v_empty[slot] : &bars->k_empty[slot];
@@ -747,14 +759,16 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       const int nA = it.n_anchor_tiles();
       const int nS = it.n_sfx_tiles();
       const int n = nA + nS;
+      const bool sh = it.template sfx_shared<FP8>();
       for (int k = 0; ok && k < n; ++k) {
         for (int q = 0; ok && q < 2; ++q) {
-          if (k >= nA || q == 0) {
-            const uint32_t seq = kv_base + pos_of(nA, q, k);
+          // shared tiles are checked once, for query tile 0 (whose group runs first)
+          if ((k >= nA && !sh) || q == 0) {
+            const uint32_t seq = kv_base + pos_of(nA, sh, q, k);
             ok = wait_parity_warp(wc, &bars->v_full[seq % C::kStages], (seq / C::kStages) & 1u);
           }
-          if (ok && k + 1 < n && (k + 1 >= nA || q == 0)) {
-            const uint32_t seq = kv_base + pos_of(nA, q, k + 1);
+          if (ok && k + 1 < n && ((k + 1 >= nA && !sh) || q == 0)) {
+            const uint32_t seq = kv_base + pos_of(nA, sh, q, k + 1);
             ok = wait_parity_warp(wc, &bars->k_full[seq % C::kStages], (seq / C::kStages) & 1u);
           }
           if (ok && arrived[q] > 0)
@@ -765,7 +779,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           __syncwarp();
         }
       }
-      kv_base += nA + 2 * nS;
+      kv_base += it.template n_tiles<FP8>();
       it = nxt;
     }
    } else if (warp == kWarpMma) {
@@ -792,6 +806,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         const int nS = it.n_sfx_tiles();
         const int nk_sfx = it.nk_sfx();
         const int n = nA + nS;
+        const bool sh = it.template sfx_shared<FP8>();
 
         // Waits (K fill, Q fill) for S(q, k) and (V fill, P ready) for PV(q, k); the MMAs
         // are issued only after every wait of the next pair of groups is done, so PV(q, k)
@@ -801,20 +816,21 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         // it a few hundred cycles while the tensor pipe reads shared memory, and the pipe's
         // queue holds only about two MMAs.
         auto wait_s = [&](int q, int k) -> bool {
-          const uint32_t seq = kv_base + pos_of(nA, q, k);
+          const uint32_t seq = kv_base + pos_of(nA, sh, q, k);
           const int slot = seq % C::kStages;
           const uint32_t ph = (seq / C::kStages) & 1u;
-          const bool sfx = k >= nA;
-          if ((sfx || q == 0) && !wait_parity_warp(wc, &bars->k_full[slot], ph)) return false;
+          const bool own = k >= nA && !sh;  // the query tile's own suffix tile
+          if ((own || q == 0) && !wait_parity_warp(wc, &bars->k_full[slot], ph))
+            return false;
           if (k == 0 && !wait_parity_warp(wc, &bars->q_full[q], it_count & 1u)) return false;
           return true;
         };
         auto wait_pv = [&](int q, int k) -> bool {
-          const uint32_t seq = kv_base + pos_of(nA, q, k);
+          const uint32_t seq = kv_base + pos_of(nA, sh, q, k);
           const int slot = seq % C::kStages;
           const uint32_t ph = (seq / C::kStages) & 1u;
-          const bool sfx = k >= nA;
-          if (FP8 && (sfx || q == 0) && !wait_parity_warp(wc, &bars->v_full[slot], ph))
+          const bool own = k >= nA && !sh;
+          if (FP8 && (own || q == 0) && !wait_parity_warp(wc, &bars->v_full[slot], ph))
             return false;
           if (!wait_parity_warp(wc, &bars->p_full[q], p_cnt[q] & 1u)) return false;
           ++p_cnt[q];
@@ -822,7 +838,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         };
         // Issue parts: called by the elected lane only.
         auto mma_s = [&](int q, int k) {
-          const uint32_t seq = kv_base + pos_of(nA, q, k);
+          const uint32_t seq = kv_base + pos_of(nA, sh, q, k);
           const int slot = seq % C::kStages;
           const bool sfx = k >= nA;
           const uint32_t k_lo = k_lo0 + slot * (2 * C::kTileBytes >> 4);
@@ -836,11 +852,11 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
             mma_ss_lohi(d_s, q_lo + adv, kDescHi, k_lo + adv, kDescHi, idesc, kk > 0 ? 1u : 0u);
           }
           mma_commit(&bars->s_full[q]);
-          if (sfx || q == 1) mma_commit(&bars->k_empty[slot]);
+          if ((k >= nA && !sh) || q == 1) mma_commit(&bars->k_empty[slot]);
           if (k == n - 1) mma_commit(&bars->q_empty[q]);
         };
         auto mma_pv = [&](int q, int k) {
-          const uint32_t seq = kv_base + pos_of(nA, q, k);
+          const uint32_t seq = kv_base + pos_of(nA, sh, q, k);
           const int slot = seq % C::kStages;
           const bool sfx = k >= nA;
           const uint32_t v_lo = v_lo0 + slot * (2 * C::kTileBytes >> 4);
@@ -857,7 +873,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
             for (int kk = 4; kk < 8; ++kk)
               mma_ts_lohi(d_o, a_p + 8u * kk, v_lo + kk * 128, kDescHi, kIdescPV, 1u);
           }
-          if (sfx || q == 1) mma_commit(&bars->v_empty[slot]);
+          if ((k >= nA && !sh) || q == 1) mma_commit(&bars->v_empty[slot]);
           if (k == n - 1) mma_commit(&bars->o_done[q]);
         };
 
@@ -884,7 +900,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
             __syncwarp();
           }
         }
-        kv_base += nA + 2 * nS;
+        kv_base += it.template n_tiles<FP8>();
         it = nxt;
       }
       // Every MMA issued so far has completed once this barrier flips.

@@ -46,6 +46,9 @@ EDGE_CASES = {
     "no_anchor_keys": ([0, 0], [3, 2], [5, 1, 17, 33, 2], (8, 2, 128)),
     "single_token_suffixes": ([40, 1000], [40, 70], (1, 1), (32, 8, 128)),
     "one_suffix": ([513], [1], [97], (32, 8, 128)),
+    # causal prefill: no anchor keys, one long sequence per anchor (shared suffix tiles)
+    "causal_prefill": ([0, 0, 0], [1, 1, 1], [700, 1, 300], (8, 2, 128)),
+    "causal_prefill_d64": ([0, 0], [1, 1], [513, 260], (16, 1, 64)),
 }
 
 

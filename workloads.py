@@ -56,6 +56,9 @@ ATTN_CONFIGS = {
     "join": AttnConfig("join", 8, (1024, 1024), 4144, (8, 24), 32, 8, 128, False, 1),
     "ragged": AttnConfig("ragged", 256, (128, 2048), 512, (4, 64), 32, 8, 128, False, 2),
     "fp8_long": AttnConfig("fp8_long", 64, (4096, 4096), 1024, (16, 96), 32, 8, 128, True, 4),
+    # causal prefill of the anchors themselves: no anchor keys, one 4,096-token sequence
+    # per "anchor" (the suffix), Qwen3-4B heads
+    "prefill": AttnConfig("prefill", 64, (0, 0), 1, (4096, 4096), 32, 8, 128, False, 6),
 }
 HEAD_CONFIGS = {
     # 64 last-token rows of the tiny attention workload plus 4,096 more rows
