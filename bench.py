@@ -40,7 +40,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="join",
-                    choices=["join", "ragged", "fp8_long", "head", "quantize"])
+                    choices=["join", "ragged", "fp8_long", "head", "quantize", "prefill"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--head-rows", type=int, default=None,
@@ -518,12 +518,65 @@ def run_bandwidth_kernel(args):
     print(json.dumps(line))
 
 
+def run_prefill(args):
+    """Per-kernel line for quail_causal_prefill_attn (the anchors' own causal prefill; not
+    the headline): 64 sequences x 4,096 tokens, 32/8 heads, d = 128. Inputs larger than L2."""
+    import prefill_only_cascade_gb300 as q
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    pk, src = peaks()
+    cfg = workloads.ATTN_CONFIGS["prefill"]
+    lay = workloads.make_layout(cfg)
+    t = workloads.make_attention_inputs(cfg, lay, dev)
+    hq, hkv, d = cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim
+    T, S, L = lay.total_suffix_tokens, lay.num_suffixes, lay.max_suffix_len
+    ws = torch.empty(q.causal_prefill_workspace_size(S, T, L, hq, hkv, d), dtype=torch.uint8,
+                     device=dev)
+    out = torch.empty(T, hq, d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(T, hq, dtype=torch.float32, device=dev)
+    run = lambda: q.causal_prefill_attn(t["q_suf"], t["k_suf"], t["v_suf"], t["suffix_offsets"],
+                                        out, L, lse=lse, workspace=ws, stream=stream)
+    for _ in range(max(args.warmup, 3)):
+        run()
+    torch.cuda.synchronize()
+    if q.get_device_error() != q.QUAIL_OK:
+        raise RuntimeError("device error during warm-up")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    with ClockSampler(0) as clk:
+        time.sleep(0.3)
+        for a, b in evs:
+            a.record(stream)
+            run()
+            b.record(stream)
+        torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    flops = attention_flops(lay, hq, d)   # 4 d Hq sum over sequences of L (L + 1) / 2
+    tflops = flops / (ms / 1e3) / 1e12
+    line = {"metric": "causal prefill tokens/sec", "value": T / (ms / 1e3), "unit": "tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
+            "higher_is_better": True, "dtype": "bf16 (fp32 accumulate)",
+            "data": "synthetic (seeded N(0,1) bf16)",
+            "config": {"workload": "prefill", "sequences": S, "sequence_len": L, "q_heads": hq,
+                       "kv_heads": hkv, "head_dim": d, "l2": "inputs larger than L2 (no flush)"},
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 2),
+                         "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(tflops / pk["bf16_tflops"], 4), "traffic": None,
+                         "peak_source": f"bf16_tflops (burst) of {src}",
+                         "kernel": "cascade_attn_kernel (anchors of length 0), one call",
+                         "algorithmic_flops_per_launch": flops},
+            "gpu_launches": 6 * args.steps, "clocks": clk.summary()}
+    print(json.dumps(line))
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
     elif args.workload in ("head", "quantize"):
         run_bandwidth_kernel(args)
+    elif args.workload == "prefill":
+        run_prefill(args)
     else:
         run_ours(args)
 

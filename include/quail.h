@@ -104,6 +104,36 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
 /* Workspace bytes that quail_cascade_attn needs for `desc` (0 when desc is NULL). */
 size_t quail_cascade_workspace_size(const quail_cascade_desc* desc);
 
+/*
+ * Causal self-attention over packed sequences: the anchors' own prefill, the step before
+ * the cascade ([P1] "Como funciona", cascade-attention bullet: the shared anchor is
+ * processed once and its KV reused by every suffix). For sequence s, token i and q-head h
+ * (KV head h / (Hq/Hkv)): softmax attention over keys 0..i of the same sequence, i.e.
+ * quail_cascade_attn with one anchor of length 0 whose suffixes are the sequences; the
+ * same kernels run.
+ *
+ *   q [T, Hq, d], k, v [T, Hkv, d]  bf16 (post-RoPE)
+ *   seq_offsets [S+1] int32 token prefix sums (monotone, seq_offsets[S] == T, every
+ *                    length <= max_seq_len; checked on the device as for the cascade)
+ *   out [T, Hq, d] bf16, 32-byte aligned; lse [T, Hq] fp32 natural log, may be NULL
+ *   softmax_scale: 0 => 1/sqrt(d)
+ *   workspace: at least quail_causal_prefill_workspace_size(...) bytes, 256-byte aligned;
+ *              overwritten (the call writes two 2-entry index arrays at its start).
+ * Errors and limits as quail_cascade_attn (d in {64, 128}, Hq/Hkv in {1, 2, 4, 8, 16}).
+ */
+quail_status quail_causal_prefill_attn(int32_t num_seqs, int64_t total_tokens,
+                                       int32_t max_seq_len, int32_t num_q_heads,
+                                       int32_t num_kv_heads, int32_t head_dim,
+                                       float softmax_scale, const void* q, const void* k,
+                                       const void* v, const int32_t* seq_offsets, void* out,
+                                       float* lse, void* workspace, size_t workspace_bytes,
+                                       quail_stream_t stream);
+
+/* Workspace bytes for quail_causal_prefill_attn (0 if the sizes are invalid). */
+size_t quail_causal_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens,
+                                           int32_t max_seq_len, int32_t num_q_heads,
+                                           int32_t num_kv_heads, int32_t head_dim);
+
 /* Size of the library's fixed device scratch array used by quail_cascade_attn_noalloc. */
 #define QUAIL_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 

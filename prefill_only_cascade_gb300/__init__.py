@@ -31,7 +31,8 @@ EXPORTED_SYMBOLS = (
     "quail_cascade_attn", "quail_cascade_workspace_size", "quail_restricted_head",
     "quail_quantize_kv_fp8", "quail_status_string", "quail_get_device_error",
     "quail_set_wait_timeout_ns", "quail_debug_inject", "quail_version",
-    "quail_cascade_attn_noalloc",
+    "quail_cascade_attn_noalloc", "quail_causal_prefill_attn",
+    "quail_causal_prefill_workspace_size",
 )
 
 
@@ -88,6 +89,12 @@ def _load():
     lib.quail_debug_inject.restype = None
     lib.quail_version.argtypes = []
     lib.quail_version.restype = ctypes.c_char_p
+    i32, i64 = ctypes.c_int32, ctypes.c_int64
+    lib.quail_causal_prefill_attn.argtypes = [i32, i64, i32, i32, i32, i32, ctypes.c_float, vp,
+                                              vp, vp, i32p, vp, f32p, vp, ctypes.c_size_t, vp]
+    lib.quail_causal_prefill_attn.restype = ctypes.c_int
+    lib.quail_causal_prefill_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32]
+    lib.quail_causal_prefill_workspace_size.restype = ctypes.c_size_t
     return lib
 
 
@@ -156,6 +163,26 @@ def cascade_attn_noalloc(desc: CascadeDesc, q_suf, k_anc, v_anc, k_suf, v_suf, a
         _ptr(anchor_offsets), _ptr(anchor_suffix_ptr), _ptr(suffix_offsets), _ptr(k_scale),
         _ptr(v_scale), _ptr(out), _ptr(lse), _stream(stream))
     _check(st, "quail_cascade_attn_noalloc")
+
+
+def causal_prefill_workspace_size(num_seqs, total_tokens, max_seq_len, num_q_heads,
+                                  num_kv_heads, head_dim):
+    return int(lib.quail_causal_prefill_workspace_size(num_seqs, total_tokens, max_seq_len,
+                                                       num_q_heads, num_kv_heads, head_dim))
+
+
+def causal_prefill_attn(q, k, v, seq_offsets, out, max_seq_len, lse=None, workspace=None,
+                        softmax_scale=0.0, stream=None):
+    """quail_causal_prefill_attn: causal self-attention over packed sequences
+    (q [T, Hq, d], k/v [T, Hkv, d] bf16, seq_offsets [S+1] int32 on the device)."""
+    if workspace is None:
+        raise ValueError("workspace is required (size: causal_prefill_workspace_size(...))")
+    st = lib.quail_causal_prefill_attn(
+        int(seq_offsets.numel() - 1), int(q.shape[0]), int(max_seq_len), int(q.shape[1]),
+        int(k.shape[1]), int(q.shape[2]), float(softmax_scale), _ptr(q), _ptr(k), _ptr(v),
+        _ptr(seq_offsets), _ptr(out), _ptr(lse), _ptr(workspace),
+        ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(stream))
+    _check(st, "quail_causal_prefill_attn")
 
 
 def restricted_head(h, gamma, w8, logits, argmax, eps=1e-6, row_index=None, n_rows=None,

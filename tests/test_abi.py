@@ -119,3 +119,32 @@ def test_quantize_rejects_bad_arguments():
     assert q.lib.quail_quantize_kv_fp8(2, None, 10, 8, 128, f, f, f, None) == q.QUAIL_ERR_INVALID_ARG
     assert q.lib.quail_quantize_kv_fp8(2, f, 10, 8, 128, ctypes.c_void_p(0x10001), f, f, None) == \
         q.QUAIL_ERR_INVALID_ARG
+
+
+def test_causal_prefill_rejects_bad_arguments():
+    f = 0x10000
+    v = lambda x: None if x is None else ctypes.c_void_p(x)
+
+    def call(S=3, T=100, L=60, hq=8, hkv=2, d=128, scale=0.0, q=f, k=f, v_=f, so=f, out=f,
+             lse=None, ws=f, ws_bytes=1 << 20):
+        return q_lib().quail_causal_prefill_attn(S, T, L, hq, hkv, d, scale, v(q), v(k), v(v_),
+                                                 v(so), v(out), v(lse), v(ws),
+                                                 ctypes.c_size_t(ws_bytes), None)
+
+    def q_lib():
+        return q.lib
+    assert call(S=-1) == q.QUAIL_ERR_INVALID_ARG
+    assert call(S=0, T=5) == q.QUAIL_ERR_INVALID_ARG
+    assert call(S=0, T=0) == q.QUAIL_OK                     # empty: nothing to do
+    assert call(hq=7) == q.QUAIL_ERR_INVALID_ARG            # not a multiple of Hkv
+    assert call(hq=6) == q.QUAIL_ERR_UNSUPPORTED            # group of 3
+    assert call(d=96) == q.QUAIL_ERR_UNSUPPORTED
+    assert call(hq=64, hkv=2) == q.QUAIL_ERR_UNSUPPORTED    # group of 32
+    assert call(scale=float("nan")) == q.QUAIL_ERR_INVALID_ARG
+    assert call(so=None) == q.QUAIL_ERR_INVALID_ARG
+    assert call(out=0x10010) == q.QUAIL_ERR_INVALID_ARG     # not 32-byte aligned
+    assert call(k=0x10008) == q.QUAIL_ERR_INVALID_ARG       # not 16-byte aligned
+    assert call(ws=0x10080) == q.QUAIL_ERR_INVALID_ARG      # workspace not 256-byte aligned
+    assert call(ws_bytes=64) == q.QUAIL_ERR_INVALID_ARG     # workspace too small
+    assert q.causal_prefill_workspace_size(3, 100, 60, 8, 2, 128) > 256
+    assert q.causal_prefill_workspace_size(-1, 100, 60, 8, 2, 128) == 0
