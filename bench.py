@@ -374,6 +374,15 @@ def run_ours(args):
                     attention_bytes(layout, hq, hkv, d, 1 if kv_fp8 else 2) /
                     (attn_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
 
+    from prefill_only_cascade_gb300 import cost_model
+    plan = cost_model.plan_report(layout.anchor_offsets, layout.anchor_suffix_ptr,
+                                  layout.suffix_offsets, hq, hkv, d, cost_model.default_hardware(),
+                                  1 if kv_fp8 else 2)
+    model = {"sol_ms": round(plan["sol_seconds"] * 1e3, 4),
+             "mma_floor_ms": round(plan["mma_floor_seconds"] * 1e3, 4),
+             "model_ms": round(plan["model_seconds"] * 1e3, 4) if not kv_fp8 else None,
+             "measured_ms": round(attn_ms, 4)}
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, q, desc, layout, t, hx, last, k_scale, v_scale, dev, stream, world)
@@ -399,7 +408,7 @@ def run_ours(args):
                    "head_dim": d, "suffix_tokens": layout.total_suffix_tokens,
                    "head_hidden": hcfg.hidden, "head_rows": S,
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "roofline": roofline, "cost_model": model, "cpu_baseline": cpu, "e2e": e2e,
         # per step: segments, schedule, items, fast + exact cascade kernels, head
         "gpu_launches": 6 * args.steps, "clocks": clk.summary(),
     }
@@ -566,6 +575,13 @@ def run_prefill(args):
                          "kernel": "cascade_attn_kernel (anchors of length 0), one call",
                          "algorithmic_flops_per_launch": flops},
             "gpu_launches": 6 * args.steps, "clocks": clk.summary()}
+    from prefill_only_cascade_gb300 import cost_model
+    plan = cost_model.plan_report(lay.anchor_offsets, lay.anchor_suffix_ptr, lay.suffix_offsets,
+                                  hq, hkv, d, cost_model.default_hardware())
+    line["cost_model"] = {"sol_ms": round(plan["sol_seconds"] * 1e3, 4),
+                          "mma_floor_ms": round(plan["mma_floor_seconds"] * 1e3, 4),
+                          "model_ms": round(plan["model_seconds"] * 1e3, 4),
+                          "measured_ms": round(ms, 4)}
     print(json.dumps(line))
 
 

@@ -1,0 +1,52 @@
+"""The cost model against live kernel times on the GPU: a reduced join plan and a reduced
+causal-prefill plan, each timed through the C ABI with CUDA events; the model must land
+within 20 % (it was calibrated on other plans' traces and times)."""
+import dataclasses
+
+import pytest
+import torch
+
+import workloads
+from parity_util import run_cascade
+from prefill_only_cascade_gb300 import cost_model as cm
+
+pytestmark = pytest.mark.gpu
+
+
+def _time(fn, reps=5):
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps / 1e3
+
+
+@pytest.mark.parametrize("name,changes", [
+    ("join", {"suffixes_per_anchor": 1024}),
+    ("prefill", {"num_anchors": 16}),
+])
+def test_model_within_20_percent(name, changes):
+    import prefill_only_cascade_gb300 as q
+    cfg = dataclasses.replace(workloads.ATTN_CONFIGS[name], **changes)
+    lay = workloads.make_layout(cfg)
+    t = workloads.make_attention_inputs(cfg, lay, "cuda")
+    heads = (cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim)
+    desc = q.make_desc(lay.num_anchors, lay.num_suffixes, lay.total_anchor_tokens,
+                       lay.total_suffix_tokens, lay.max_anchor_len, lay.max_suffix_len, *heads)
+    ws = torch.empty(q.cascade_workspace_size(desc), dtype=torch.uint8, device="cuda")
+    out = torch.empty(lay.total_suffix_tokens, cfg.num_q_heads, cfg.head_dim,
+                      dtype=torch.bfloat16, device="cuda")
+    run = lambda: q.cascade_attn(desc, t["q_suf"], t["k_anc"], t["v_anc"], t["k_suf"],
+                                 t["v_suf"], t["anchor_offsets"], t["anchor_suffix_ptr"],
+                                 t["suffix_offsets"], out, None, ws)
+    measured = _time(run)
+    assert q.get_device_error() == q.QUAIL_OK
+    model = cm.kernel_seconds(lay.anchor_offsets, lay.anchor_suffix_ptr, lay.suffix_offsets,
+                              *heads, cm.default_hardware())["seconds"]
+    print(name, "measured %.3f ms, model %.3f ms" % (measured * 1e3, model * 1e3))
+    assert abs(model / measured - 1) < 0.20
