@@ -25,6 +25,10 @@ Readings where the pages are silent (each also listed in the design notes):
   fp32 scale per (anchor, KV head) = amax / 448 (1 when amax == 0), codes by
   round-to-nearest-even with saturation from the fp32 quotient x / scale.
 
+kv_plan.py: the anchor-KV cache plan of a known query plan (LRU, furthest-next-use,
+and the exhaustive minimum regret); pins in tests/test_oracle_kv_plan.py (a hand-worked
+plan, furthest-next-use equal to the exhaustive minimum for equal sizes, bounds).
+
 Pins (tests/test_oracle.py): brute-force loops, the cascade-merge = monolithic identity,
 closed forms, a library SDPA with an explicit mask, RMSNorm closed forms, all 256 E4M3
 codes against the OCP formula and against torch's float8_e4m3fn. No function here is
