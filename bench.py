@@ -40,7 +40,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="join",
-                    choices=["join", "ragged", "fp8_long", "head", "quantize", "prefill"])
+                    choices=["join", "ragged", "fp8_long", "head", "quantize", "prefill",
+                             "kvplan"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--head-rows", type=int, default=None,
@@ -585,6 +586,33 @@ def run_prefill(args):
     print(json.dumps(line))
 
 
+def run_kvplan(args):
+    """Query-aware anchor-KV cache plan (host code, no GPU): regret tokens of a general
+    server's LRU against furthest-next-use on seeded synthetic join plans, and the
+    planner's throughput. One JSON line; value = furthest-next-use regret on the zipf plan."""
+    import prefill_only_cascade_gb300 as q
+    res = {}
+    for name, cfg in workloads.KV_PLAN_CONFIGS.items():
+        acc, size, cap = workloads.make_kv_plan(cfg)
+        row = {"accesses": int(acc.size), "anchors": int(size.size), "capacity_tokens": cap}
+        for pol, label in ((q.KV_LRU, "lru"), (q.KV_FURTHEST_NEXT_USE, "furthest_next_use")):
+            t0 = time.perf_counter()
+            for _ in range(max(args.steps, 1)):
+                _, st = q.kv_plan(acc, size, cap, pol)
+            dt = (time.perf_counter() - t0) / max(args.steps, 1)
+            row[label] = {"regret_tokens": st["regret_tokens"], "hits": st["hits"],
+                          "accesses_per_s": acc.size / dt}
+            row["compulsory_tokens"] = st["compulsory_tokens"]
+        res[name] = row
+    z = res["zipf"]
+    line = {"metric": "KV regret tokens (query-aware anchor cache, zipf plan)",
+            "value": z["furthest_next_use"]["regret_tokens"], "unit": "tokens",
+            "higher_is_better": False, "n_gpus": 0, "steps": max(args.steps, 1),
+            "data": "synthetic seeded join plans", "config": {"workload": "kvplan"},
+            "plans": res}
+    print(json.dumps(line))
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -593,6 +621,8 @@ def main():
         run_bandwidth_kernel(args)
     elif args.workload == "prefill":
         run_prefill(args)
+    elif args.workload == "kvplan":
+        run_kvplan(args)
     else:
         run_ours(args)
 

@@ -134,6 +134,37 @@ size_t quail_causal_prefill_workspace_size(int32_t num_seqs, int64_t total_token
                                            int32_t max_seq_len, int32_t num_q_heads,
                                            int32_t num_kv_heads, int32_t head_dim);
 
+/*
+ * Query-aware anchor-KV cache plan ([P1] "Como funciona", first bullet: the whole query
+ * plan is known in advance, so KV can be evicted without regret; the KV-regret paragraph of
+ * "Quail, il motore di inferenza che supera il miliardo di token al minuto su una H100").
+ * HOST call on HOST memory (the one exception to the device-pointer rule; no GPU work).
+ *
+ *   anchor_tokens [num_anchors] KV size of each anchor in tokens (>= 0)
+ *   access_anchor [num_accesses] the plan's anchor accesses in execution order (0..A-1)
+ *   capacity_tokens  tokens of anchor KV the GPU may hold
+ *   policy       QUAIL_KV_LRU (oldest last access is evicted; always inserts) or
+ *                QUAIL_KV_FURTHEST_NEXT_USE (the resident - or the incoming anchor, which
+ *                is then bypassed - whose next access is furthest; ties: larger size, then
+ *                larger id)
+ *   hit          [num_accesses] out: 1 = the anchor's KV was resident; may be NULL
+ *   stats        out: hits, misses, compulsory tokens (first prefill of each anchor),
+ *                regret tokens (prefilled again after an eviction or bypass), peak
+ *                resident tokens. An anchor larger than the capacity is never resident.
+ * Errors: QUAIL_ERR_INVALID_ARG for negative counts or sizes, ids out of range, NULL
+ * inputs with nonzero counts, NULL stats or an unknown policy.
+ */
+typedef enum { QUAIL_KV_LRU = 0, QUAIL_KV_FURTHEST_NEXT_USE = 1 } quail_kv_policy;
+typedef struct {
+  int64_t hits, misses;
+  int64_t compulsory_tokens, regret_tokens;
+  int64_t peak_resident_tokens;
+} quail_kv_plan_stats;
+quail_status quail_kv_plan(int32_t num_anchors, const int64_t* anchor_tokens,
+                           int64_t num_accesses, const int32_t* access_anchor,
+                           int64_t capacity_tokens, int32_t policy, uint8_t* hit,
+                           quail_kv_plan_stats* stats);
+
 /* Size of the library's fixed device scratch array used by quail_cascade_attn_noalloc. */
 #define QUAIL_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 

@@ -32,7 +32,7 @@ EXPORTED_SYMBOLS = (
     "quail_quantize_kv_fp8", "quail_status_string", "quail_get_device_error",
     "quail_set_wait_timeout_ns", "quail_debug_inject", "quail_version",
     "quail_cascade_attn_noalloc", "quail_causal_prefill_attn",
-    "quail_causal_prefill_workspace_size",
+    "quail_causal_prefill_workspace_size", "quail_kv_plan",
 )
 
 
@@ -40,6 +40,15 @@ class QuailError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
         super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class KvPlanStats(ctypes.Structure):
+    _fields_ = [("hits", ctypes.c_int64), ("misses", ctypes.c_int64),
+                ("compulsory_tokens", ctypes.c_int64), ("regret_tokens", ctypes.c_int64),
+                ("peak_resident_tokens", ctypes.c_int64)]
+
+
+KV_LRU, KV_FURTHEST_NEXT_USE = 0, 1
 
 
 class CascadeDesc(ctypes.Structure):
@@ -95,6 +104,8 @@ def _load():
     lib.quail_causal_prefill_attn.restype = ctypes.c_int
     lib.quail_causal_prefill_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32]
     lib.quail_causal_prefill_workspace_size.restype = ctypes.c_size_t
+    lib.quail_kv_plan.argtypes = [i32, vp, i64, vp, i64, i32, vp, ctypes.POINTER(KvPlanStats)]
+    lib.quail_kv_plan.restype = ctypes.c_int
     return lib
 
 
@@ -183,6 +194,20 @@ def causal_prefill_attn(q, k, v, seq_offsets, out, max_seq_len, lse=None, worksp
         _ptr(seq_offsets), _ptr(out), _ptr(lse), _ptr(workspace),
         ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(stream))
     _check(st, "quail_causal_prefill_attn")
+
+
+def kv_plan(access_anchor, anchor_tokens, capacity_tokens, policy=KV_FURTHEST_NEXT_USE):
+    """quail_kv_plan on host arrays: returns (hit flags uint8 [accesses], stats dict)."""
+    import numpy as np
+    acc = np.ascontiguousarray(access_anchor, dtype=np.int32)
+    size = np.ascontiguousarray(anchor_tokens, dtype=np.int64)
+    hit = np.zeros(acc.size, dtype=np.uint8)
+    st = KvPlanStats()
+    code = lib.quail_kv_plan(int(size.size), size.ctypes.data, int(acc.size), acc.ctypes.data,
+                             int(capacity_tokens), int(policy), hit.ctypes.data,
+                             ctypes.byref(st))
+    _check(code, "quail_kv_plan")
+    return hit, {f: getattr(st, f) for f, _ in KvPlanStats._fields_}
 
 
 def restricted_head(h, gamma, w8, logits, argmax, eps=1e-6, row_index=None, n_rows=None,

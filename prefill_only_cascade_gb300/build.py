@@ -17,7 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libquail.so")
-SOURCES = ["api.cu", "cascade.cu", "head.cu", "noalloc.cu", "prefill.cu", "quantize.cu"]
+SOURCES = ["api.cu", "cascade.cu", "head.cu", "kv_plan.cu", "noalloc.cu", "prefill.cu",
+           "quantize.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -231,3 +231,39 @@ def _to_np(t: torch.Tensor) -> np.ndarray:
     if t.dtype == torch.bfloat16:
         return t.to(torch.float32).numpy()
     return t.numpy()
+
+
+@dataclass(frozen=True)
+class KvPlanConfig:
+    name: str
+    num_anchors: int
+    anchor_tokens: tuple   # inclusive (lo, hi)
+    kind: str              # "two_pass" or "zipf"
+    accesses: int          # zipf only
+    capacity_frac: float   # anchor-KV capacity as a fraction of all anchors' tokens
+    seed: int
+
+
+KV_PLAN_CONFIGS = {
+    # the join of the BIO-4 shape: every anchor's KV is needed in two passes over the
+    # anchors (the second list read twice), same order both times
+    "two_pass": KvPlanConfig("two_pass", 5000, (256, 1024), "two_pass", 0, 0.15, 7),
+    # several queries over shared tables: anchor popularity Zipf(1.1)
+    "zipf": KvPlanConfig("zipf", 2000, (256, 1024), "zipf", 40000, 0.15, 8),
+}
+
+
+def make_kv_plan(cfg: KvPlanConfig):
+    """Seeded anchor sizes (tokens), access sequence and capacity of a synthetic plan."""
+    rng = np.random.default_rng(cfg.seed)
+    size = rng.integers(cfg.anchor_tokens[0], cfg.anchor_tokens[1] + 1, size=cfg.num_anchors)
+    if cfg.kind == "two_pass":
+        order = np.arange(cfg.num_anchors)
+        acc = np.concatenate([order, order])
+    else:
+        ranks = np.arange(1, cfg.num_anchors + 1, dtype=np.float64)
+        p = ranks ** -1.1
+        acc = rng.choice(cfg.num_anchors, size=cfg.accesses, p=p / p.sum())
+    capacity = int(cfg.capacity_frac * size.sum())
+    return acc.astype(np.int32), size.astype(np.int64), capacity
+
