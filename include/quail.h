@@ -65,7 +65,7 @@ typedef struct {
   int32_t num_kv_heads;          /* Hkv */
   int32_t head_dim;              /* d: 64 or 128 */
   float softmax_scale;           /* 0 => 1/sqrt(d) */
-  int32_t kv_anchor_dtype;       /* quail_dtype of k_anc/v_anc; FP8_E4M3 needs d = 128 */
+  int32_t kv_anchor_dtype;       /* quail_dtype of k_anc/v_anc */
 } quail_cascade_desc;
 
 /*
@@ -88,7 +88,9 @@ typedef struct {
  *   lse     [T_S, Hq] fp32 natural log of the sum of exp(scaled scores); may be NULL
  *   workspace: device scratch of at least quail_cascade_workspace_size(desc) bytes,
  *              16-byte aligned; its contents are overwritten. Calls that share one
- *              workspace must not overlap on the GPU.
+ *              workspace must not overlap on the GPU. With FP8_E4M3 it also holds the
+ *              anchor codes widened to bf16 (exact), 4 * T_A * Hkv * d bytes, which
+ *              the attention reads in place of the codes.
  * Empty inputs are legal (S = 0, anchors without suffixes, L_a = 0 where lse of the
  * anchor part is -inf). Supported: d in {64, 128}, Hq/Hkv in {1, 2, 4, 8, 16}.
  */

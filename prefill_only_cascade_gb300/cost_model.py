@@ -150,22 +150,32 @@ def masked_tiles(items: dict) -> np.ndarray:
     return 2 * (n_sfx + (la % KEYS != 0))
 
 
+def staging_seconds(anchor_offsets, hkv: int, d: int, hw: Hardware = Hardware()) -> float:
+    """FP8 anchor KV: time of the pass that widens the e4m3 anchor K and V codes to bf16
+    (1 byte read and 2 written per code) at the HBM peak."""
+    ta = int(np.asarray(anchor_offsets, dtype=np.int64)[-1])
+    return 2.0 * ta * hkv * d * 3 / (hw.hbm_gbs * 1e9)
+
+
 def kernel_seconds(anchor_offsets, anchor_suffix_ptr, suffix_offsets, hq: int, hkv: int,
-                   d: int, hw: Hardware = Hardware()) -> dict:
-    """Modelled time of one quail_cascade_attn call (BF16 path): items round-robin over
+                   d: int, hw: Hardware = Hardware(), fp8: bool = False) -> dict:
+    """Modelled time of one quail_cascade_attn call: items round-robin over
     min(items, SMs) persistent CTAs; each costs its MMA cycles / step_efficiency, the
     per-item overhead and the masked-tile cost; the call takes the slowest CTA plus the
-    launch overhead."""
+    launch overhead (and, with FP8 anchor KV, the bf16 staging pass: the attention
+    kernel is then the BF16 one)."""
     items = work_items(anchor_offsets, anchor_suffix_ptr, suffix_offsets, hq, hkv)
     n = items["la"].size
+    extra = staging_seconds(anchor_offsets, hkv, d, hw) if fp8 else 0.0
     if n == 0:
-        return {"seconds": hw.launch_overhead_us * 1e-6, "items": 0, "mma_cycles": 0.0}
+        return {"seconds": hw.launch_overhead_us * 1e-6 + extra, "items": 0, "mma_cycles": 0.0}
     mma = item_mma_cycles(items, d, hw)
     cyc = (mma / hw.step_efficiency + hw.item_overhead_cycles
            + masked_tiles(items) * hw.masked_tile_cycles)
     grid = min(n, hw.sm_count)
     per_cta = np.bincount(np.arange(n) % grid, weights=cyc, minlength=grid)
-    seconds = float(per_cta.max()) / (hw.sm_clock_ghz * 1e9) + hw.launch_overhead_us * 1e-6
+    seconds = (float(per_cta.max()) / (hw.sm_clock_ghz * 1e9) + hw.launch_overhead_us * 1e-6
+               + extra)
     return {"seconds": seconds, "items": int(n), "mma_cycles": float(mma.sum()),
             "mma_floor_seconds": float(np.bincount(np.arange(n) % grid, weights=mma,
                                                    minlength=grid).max())
@@ -176,7 +186,8 @@ def plan_report(anchor_offsets, anchor_suffix_ptr, suffix_offsets, hq: int, hkv:
                 hw: Hardware = Hardware(), kv_bytes: int = 2) -> dict:
     """Work, speed-of-light time and modelled kernel time of one call, in one dict."""
     w = work(anchor_offsets, anchor_suffix_ptr, suffix_offsets, hq, hkv, d, kv_bytes)
-    k = kernel_seconds(anchor_offsets, anchor_suffix_ptr, suffix_offsets, hq, hkv, d, hw)
+    k = kernel_seconds(anchor_offsets, anchor_suffix_ptr, suffix_offsets, hq, hkv, d, hw,
+                       fp8=kv_bytes == 1)
     sol = sol_seconds(w["flops"], w["bytes"], hw)
     return {**w, "sol_seconds": sol, "model_seconds": k["seconds"], "items": k["items"],
             "mma_floor_seconds": k.get("mma_floor_seconds", 0.0),

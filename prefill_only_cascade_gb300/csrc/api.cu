@@ -122,6 +122,14 @@ void quail_debug_inject(int32_t skip_first_kv_load) {
   g_inject_skip = skip_first_kv_load != 0;
 }
 
+// FP8 anchor KV: bytes of each bf16 copy of the anchor codes staged in the workspace.
+static int64_t anchor_bf16_bytes(const quail_cascade_desc& d) {
+  if (d.kv_anchor_dtype != QUAIL_FP8_E4M3 || d.total_anchor_tokens <= 0 ||
+      (d.head_dim != 64 && d.head_dim != 128))
+    return 0;
+  return d.total_anchor_tokens * d.num_kv_heads * d.head_dim * 2;
+}
+
 size_t quail_cascade_workspace_size(const quail_cascade_desc* desc) {
   if (desc == nullptr || desc->num_anchors < 0 || desc->total_suffix_tokens < 0 ||
       desc->num_q_heads <= 0 || desc->num_kv_heads <= 0 ||
@@ -131,7 +139,9 @@ size_t quail_cascade_workspace_size(const quail_cascade_desc* desc) {
   const int64_t bound = quail::cascade_item_bound(
       desc->num_anchors, desc->total_suffix_tokens, desc->num_kv_heads,
       desc->num_q_heads / desc->num_kv_heads);
-  return quail::cascade_workspace_layout(desc->num_anchors, desc->total_suffix_tokens, bound).total;
+  return quail::cascade_workspace_layout(desc->num_anchors, desc->total_suffix_tokens, bound,
+                                         anchor_bf16_bytes(*desc))
+      .total;
 }
 
 quail_status quail_get_device_error(quail_stream_t stream) {
@@ -178,7 +188,6 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
   const int group = d.num_q_heads / d.num_kv_heads;
   if (d.head_dim != 64 && d.head_dim != 128) return QUAIL_ERR_UNSUPPORTED;
   if (!valid_group(group)) return QUAIL_ERR_UNSUPPORTED;
-  if (fp8 && d.head_dim != 128) return QUAIL_ERR_UNSUPPORTED;
   if (anchor_offsets == nullptr || anchor_suffix_ptr == nullptr || suffix_offsets == nullptr)
     return QUAIL_ERR_INVALID_ARG;
   if (d.total_suffix_tokens > 0) {
@@ -199,8 +208,8 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
   const int64_t item_bound =
       quail::cascade_item_bound(d.num_anchors, d.total_suffix_tokens, d.num_kv_heads, group);
   if (item_bound > (1ll << 31) - 1) return QUAIL_ERR_UNSUPPORTED;
-  const quail::CascadeWorkspace wl =
-      quail::cascade_workspace_layout(d.num_anchors, d.total_suffix_tokens, item_bound);
+  const quail::CascadeWorkspace wl = quail::cascade_workspace_layout(
+      d.num_anchors, d.total_suffix_tokens, item_bound, anchor_bf16_bytes(d));
   if (workspace == nullptr || workspace_bytes < wl.total || !aligned16(workspace))
     return QUAIL_ERR_INVALID_ARG;
 
@@ -214,16 +223,19 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
   quail::CascadeMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  // The FP8 variant loads its tiles without TMA; the maps are then unused.
-  bool ok = fp8 ||
-            (encode_3d(&maps.q, q_suf, d.total_suffix_tokens, d.num_q_heads, D, group, tok, bf, 2, 64) &&
-             encode_3d(&maps.k_suf, k_suf, d.total_suffix_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64) &&
-             encode_3d(&maps.v_suf, v_suf, d.total_suffix_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64));
-  if (fp8) {
-    // nothing to encode
-  } else if (d.total_anchor_tokens > 0) {
-    ok = ok && encode_3d(&maps.k_anc, k_anc, d.total_anchor_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64) &&
-         encode_3d(&maps.v_anc, v_anc, d.total_anchor_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64);
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  // FP8 anchor KV: the kernels read the bf16 copies that the staging kernel writes into
+  // the workspace.
+  const void* k_anc_tiles = fp8 ? static_cast<const void*>(wsb + wl.k_anc_bf16) : k_anc;
+  const void* v_anc_tiles = fp8 ? static_cast<const void*>(wsb + wl.v_anc_bf16) : v_anc;
+  bool ok =
+      encode_3d(&maps.q, q_suf, d.total_suffix_tokens, d.num_q_heads, D, group, tok, bf, 2, 64) &&
+      encode_3d(&maps.k_suf, k_suf, d.total_suffix_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64) &&
+      encode_3d(&maps.v_suf, v_suf, d.total_suffix_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64);
+  if (d.total_anchor_tokens > 0) {
+    ok = ok &&
+         encode_3d(&maps.k_anc, k_anc_tiles, d.total_anchor_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64) &&
+         encode_3d(&maps.v_anc, v_anc_tiles, d.total_anchor_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64);
   } else {
     maps.k_anc = maps.k_suf;  // never read: every anchor is empty
     maps.v_anc = maps.v_suf;
@@ -257,7 +269,6 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
   p.out = out;
   p.lse = lse;
   p.item_bound = static_cast<int>(item_bound);
-  uint8_t* wsb = static_cast<uint8_t*>(workspace);
   p.flag = reinterpret_cast<int32_t*>(wsb + wl.flag);
   p.prefix = reinterpret_cast<int32_t*>(wsb + wl.prefix);
   p.order = reinterpret_cast<int32_t*>(wsb + wl.order);
@@ -266,6 +277,8 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
   p.redo_count = reinterpret_cast<int32_t*>(wsb + wl.redo_count);
   p.redo_flag = reinterpret_cast<int32_t*>(wsb + wl.redo_flag);
   p.redo_list = reinterpret_cast<int32_t*>(wsb + wl.redo_list);
+  p.k_anc_bf16 = fp8 ? wsb + wl.k_anc_bf16 : nullptr;
+  p.v_anc_bf16 = fp8 ? wsb + wl.v_anc_bf16 : nullptr;
   p.err_word = st->err_word;
   {
     std::lock_guard<std::mutex> lock(g_mutex);

@@ -22,28 +22,29 @@
 //   3. cascade_schedule_kernel  (1 CTA)  anchor checks; anchors ordered by decreasing
 //                                        anchor-tile count; prefix sum of work items
 //   4. cascade_items_kernel     (grid)   one 32-byte record per work item
-//   5. cascade_attn_kernel      (persistent, one CTA per SM)
+//   5. anchor_e4m3_to_bf16_kernel (grid, FP8 anchor KV only) stages the anchor codes as
+//                                        bf16 in the workspace
+//   6. cascade_attn_kernel      (persistent, one CTA per SM), fast then exact instance
 //
 // Per CTA of the attention kernel:
 //   warp 8      TMA producer: Q tiles, then a ring of K / V tiles (128 keys each)
 //   warp 9      MMA issuer:   S_q = Q_q K^T (SMEM x SMEM -> TMEM), O_q += P_q V
 //                             (P from TMEM, V from SMEM), tcgen05 kind::f16, M = 128
+//   warp 10     fill checker: folds the V and next-K fills into the P-ready barrier
 //   warps 0-3   softmax of query tile 0, one thread per TMEM lane (= query row)
 //   warps 4-7   softmax of query tile 1
-//   warps 10-11 idle (they complete the third warpgroup for the register split)
+//   warp 11     idle (it completes the third warpgroup for the register split)
 // TMEM (512 columns): tile q uses S/P at columns 256q .. +127 and O at 256q+128 .. +255.
 // The two query tiles share every anchor KV tile loaded into shared memory and ping-pong:
 // while one warpgroup exponentiates its scores the tensor core works on the other tile.
 //
 // FP8 anchor KV (e4m3 codes with one fp32 scale per (anchor, KV head) for K and for V):
-// the same kernel with FP8 = true. tcgen05 kind::f16 needs both operands of one type and
-// there is no exact e4m3 -> bf16 conversion instruction, while e4m3 -> f16 is exact, so
-// this variant runs its MMAs in f16: warps 8, 10 and 11 load every tile with plain
-// 16-byte loads (anchor codes e4m3, Q and suffix K/V bf16), convert to f16 (exact for
-// e4m3; bf16 -> f16 is exact for |x| in [2^-14, 65504] and saturates above) and store it
-// in the same 128-byte-swizzled operand layout that TMA produces. The K scale folds into
-// the score scale of anchor tiles and the V scale into their P (P = p * v_scale, while the
-// row sum keeps p), so O accumulates true values; P is stored as f16.
+// every e4m3 value is a bf16 value, so the codes are widened to bf16 once per call into
+// the workspace (exact; 2 bytes written per code) and the same bf16 kernel runs with
+// FP8 = true. The K scale folds into the score scale of anchor tiles and the V scale into
+// their P (P = p * v_scale, while the row sum keeps p), so O accumulates true values.
+// Converting once per call instead of once per work item keeps the tensor core fed: a
+// (anchor, KV head) is read by hundreds of work items.
 #include <algorithm>
 
 #include <cuda_bf16.h>
@@ -66,19 +67,18 @@ constexpr int kThreads = 384;             // three warpgroups
 // holds; the host checks the compiled register count before launching.
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
-constexpr int kWarpFillCheck = 10;  // BF16 variant (the FP8 variant uses warp 10 to load)
+constexpr int kWarpFillCheck = 10;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: O is rescaled only past 2^8
 // Fast kernel bounds (P = 2^(s c) with no max subtracted); outside them the item goes to
-// the exact kernel.
-//  * bf16 P: the row sum l = sum P must lie in [2^-64, 2^32]. Every P <= l <= 2^32 keeps O
-//    and l far from fp32 overflow (an infinite P makes l infinite, so it is caught), and
-//    l >= 2^-64 keeps the largest P >= 2^-64 / (keys), far inside the bf16/fp32 range.
-//    Testing l needs no row max at all.
-//  * f16 P (FP8 variant, times v_scale): the row max of s c must lie in [-8, 8]: P stays
-//    below 65504 and its largest value is not pushed toward the f16 subnormals.
+// the exact kernel. The row sum l = sum P must lie in [2^-64, 2^32]: every P <= l <= 2^32
+// keeps O and l far from fp32 overflow (an infinite P makes l infinite, so it is caught),
+// and l >= 2^-64 keeps the largest P >= 2^-64 / (keys), far inside the bf16/fp32 range.
+// Testing l needs no row max at all. With FP8 anchor KV, P also carries v_scale; a scale
+// above 2^64 (or NaN) sends the item to the exact kernel as well, so P * v_scale and O
+// stay finite.
 constexpr float kSpecSumLow = 5.421010862427522e-20f;   // 2^-64
 constexpr float kSpecSumHigh = 4294967296.0f;            // 2^32
-constexpr float kSpecMaxF16 = 8.0f;
+constexpr float kSpecScaleHigh = 1.8446744073709552e19f;  // 2^64
 constexpr int kSortBins = 1024;
 constexpr uint32_t kTmemCols = 512;
 
@@ -95,14 +95,6 @@ struct Cfg {
   static constexpr int kRegsOther = (D == 128) ? 152 : 136;
   static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= 384 * 168, "register split");
 };
-// The FP8 variant's loader warps (in the third warpgroup) need more registers.
-template <int D, bool FP8>
-struct Regs {
-  static constexpr int kSoftmax = FP8 ? 168 : Cfg<D>::kRegsSoftmax;
-  static constexpr int kOther = FP8 ? 168 : Cfg<D>::kRegsOther;
-  static_assert(256 * kSoftmax + 128 * kOther <= 384 * 168, "register split");
-};
-
 struct __align__(8) Bars {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
@@ -110,7 +102,6 @@ struct __align__(8) Bars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
-  int loader_ok;  // FP8 variant: result of the loader leader's wait, read by all loaders
 };
 
 // One work item as written by cascade_items_kernel (two int4).
@@ -128,14 +119,11 @@ struct Item {
     return (n_sfx_tiles() == 1 && window() <= 64) ? 64 : 128;
   }
   // Both query tiles' suffix windows start at the same token (both inside one suffix, or
-  // q1 inside the suffix where q0 ends): then the BF16 variant lets them share their
-  // suffix tiles as they share the anchor tiles (q0 masks the keys past its rows). The FP8
-  // variant keeps them separate (measured faster there).
-  template <bool FP8>
-  __device__ __forceinline__ bool sfx_shared() const { return !FP8 && ws0 == ws1; }
-  template <bool FP8>
+  // q1 inside the suffix where q0 ends): then they share their suffix tiles as they share
+  // the anchor tiles (q0 masks the keys past its rows).
+  __device__ __forceinline__ bool sfx_shared() const { return ws0 == ws1; }
   __device__ __forceinline__ int n_tiles() const {
-    return n_anchor_tiles() + (sfx_shared<FP8>() ? 1 : 2) * n_sfx_tiles();
+    return n_anchor_tiles() + (sfx_shared() ? 1 : 2) * n_sfx_tiles();
   }
 };
 
@@ -209,149 +197,22 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-template <bool F16>
-__device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
-  return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
-}
-
-// ------------------------------------------------------------ FP8-variant tile loaders
-constexpr int kLoaderThreads = 96;  // warps 8, 10, 11
-
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-  return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-}
-// Four e4m3 codes (bytes 0..3 of w) -> two f16x2 words (codes 0,1 and codes 2,3; the lower
-// code in the lower half). Exact: every e4m3 value is an f16 value.
-__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& a, uint32_t& b) {
-  asm("{\n\t.reg .b16 lo, hi;\n\t"
-      "mov.b32 {lo, hi}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
-      : "=r"(a), "=r"(b)
-      : "r"(w));
-}
-// Byte offset of 16-byte chunk `jp` (8 f16 / bf16 elements, counted along the row across
-// 64-element blocks) of row r in a 128-byte-swizzled tile of 128-row blocks.
-__device__ __forceinline__ uint32_t sw128_offset(int r, int jp) {
-  return static_cast<uint32_t>((jp >> 3) * 16384 + r * 128 + (((jp & 7) ^ (r & 7)) << 4));
-}
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-__device__ __forceinline__ uint4 ld_nc_u4(const uint8_t* p, uint64_t policy) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p), "l"(policy));
-  return v;
-}
-__device__ __forceinline__ int clamp_rows(int64_t v, int hi) {
-  return v < 0 ? 0 : (v > hi ? hi : static_cast<int>(v));
-}
 // 32-byte global store (sm_100+); p must be 32-byte aligned.
 __device__ __forceinline__ void st_global_v8(void* p, const uint32_t* v) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
                "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
 }
-__device__ __forceinline__ void loader_bar() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kLoaderThreads) : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// bf16 rows -> f16 tile rows [0, rows). Row r of the source starts at
-//   base + (r >> gshift) * tok_stride + (r & (G - 1)) * head_stride  (bytes, d = 128)
-// and rows >= valid_rows read as zero. Done in two halves to bound the loads in flight.
-__device__ __forceinline__ void load_tile_bf16(uint32_t tile, const uint8_t* base,
-                                               int64_t tok_stride, int gshift,
-                                               int64_t head_stride, int rows, int valid_rows,
-                                               int lt, uint64_t policy) {
-  constexpr int kHalf = (64 * 16 + kLoaderThreads - 1) / kLoaderThreads;
-  const int units = rows * 16;
-  const int gmask = (1 << gshift) - 1;
-#pragma unroll 1
-  for (int h = 0; h < 2; ++h) {
-    uint4 v[kHalf];
-#pragma unroll
-    for (int i = 0; i < kHalf; ++i) {
-      const int u = h * 1024 + lt + i * kLoaderThreads;
-      v[i] = make_uint4(0u, 0u, 0u, 0u);
-      const int r = u >> 4;
-      if (u < min(units, (h + 1) * 1024) && r < valid_rows)
-        v[i] = ld_nc_u4(base + (r >> gshift) * tok_stride + (r & gmask) * head_stride +
-                        (u & 15) * 16, policy);
-    }
-#pragma unroll
-    for (int i = 0; i < kHalf; ++i) {
-      const int u = h * 1024 + lt + i * kLoaderThreads;
-      if (u < min(units, (h + 1) * 1024)) {
-        const uint4 o = make_uint4(bf16x2_to_f16x2(v[i].x), bf16x2_to_f16x2(v[i].y),
-                                   bf16x2_to_f16x2(v[i].z), bf16x2_to_f16x2(v[i].w));
-        st_shared_v4(tile + sw128_offset(u >> 4, u & 15), o);
-      }
-    }
-  }
-}
-
-// e4m3 rows (128 codes each, row r at base + r * row_stride) -> f16 tile, in two phases so
-// that the loads of one tile can be in flight while another tile is converted: rows >=
-// valid_rows read as zero.
-//
-// Unit u (16 codes) -> row and 16-code column c chosen so that the 32 lanes of one warp
-// instruction cover 8 rows x 4 columns: with the 128-byte swizzle their 16-byte stores then
-// spread evenly over the 8 bank groups (4 lanes each, the minimum for 512 bytes).
-constexpr int kE4m3PerThread = (128 * 8 + kLoaderThreads - 1) / kLoaderThreads;
-__device__ __forceinline__ int e4m3_row(int u) { return (u >> 6) * 8 + ((u & 31) >> 2); }
-__device__ __forceinline__ int e4m3_col(int u) { return (u & 3) + 4 * ((u >> 5) & 1); }
-__device__ __forceinline__ void load_e4m3_regs(uint4 (&v)[kE4m3PerThread], const uint8_t* base,
-                                               int64_t row_stride, int valid_rows, int lt,
-                                               uint64_t policy) {
-#pragma unroll
-  for (int i = 0; i < kE4m3PerThread; ++i) {
-    const int u = lt + i * kLoaderThreads;
-    v[i] = make_uint4(0u, 0u, 0u, 0u);
-    const int r = e4m3_row(u);
-    if (u < 1024 && r < valid_rows)
-      v[i] = ld_nc_u4(base + r * row_stride + e4m3_col(u) * 16, policy);
-  }
-}
-__device__ __forceinline__ void store_e4m3_regs(uint32_t tile, const uint4 (&v)[kE4m3PerThread],
-                                                int lt) {
-#pragma unroll
-  for (int i = 0; i < kE4m3PerThread; ++i) {
-    const int u = lt + i * kLoaderThreads;
-    if (u < 1024) {
-      const int r = e4m3_row(u), c = e4m3_col(u);  // codes d = 16c .. 16c + 15
-      uint4 lo, hi;
-      e4m3x4_to_f16x4(v[i].x, lo.x, lo.y);
-      e4m3x4_to_f16x4(v[i].y, lo.z, lo.w);
-      e4m3x4_to_f16x4(v[i].z, hi.x, hi.y);
-      e4m3x4_to_f16x4(v[i].w, hi.z, hi.w);
-      st_shared_v4(tile + sw128_offset(r, 2 * c), lo);
-      st_shared_v4(tile + sw128_offset(r, 2 * c + 1), hi);
-    }
-  }
-}
 
 // ---------------------------------------------------------------------------------
 // Softmax of one S tile: one thread per row, NC columns; P = 2^(s c - m) is written back
-// to TMEM (bf16 pairs; f16 times pscale in the FP8 variant, pscale = v_scale on anchor
-// tiles) over the upper half of the S columns, and l accumulates the unscaled P.
+// to TMEM as bf16 pairs (times pscale = v_scale on the anchor tiles of the FP8 variant)
+// over the upper half of the S columns, and l accumulates the unscaled P.
 //
 // Two kernels share this code:
 //  * the fast kernel uses m = 0 throughout: no max pass and no rescale of O. An item with
 //    a valid row outside the fast-kernel bounds (P could overflow, or all of it
-//    underflow: tested on l for bf16 P, on the row max - computed alongside the
-//    exponentials - for f16 P) is listed for the exact kernel, which writes its output
+//    underflow: tested on l) is listed for the exact kernel, which writes its output
 //    rows again;
 //  * the exact kernel recomputes those items with the usual online softmax (lazy rescale
 //    of O past 2^kRescaleThreshold).
@@ -374,39 +235,33 @@ __device__ __forceinline__ void load_s(uint32_t t_s, bool masked, int lo_c, int 
   }
 }
 
-// P = 2^(s c - m_safe) for all NC columns, packed in pairs and stored to TMEM at t_p
-// 32 columns (16 packed) at a time as they are made; returns the row sum of P and, if
-// WITH_MAX, the row max of s (8 independent chains of 3-input maxes, off the exp path).
-template <int NC, bool F16P, bool WITH_MAX>
+// P = 2^(s c - m_safe) for all NC columns, packed in bf16 pairs (times pscale if SCALED)
+// and stored to TMEM at t_p 32 columns (16 packed) at a time as they are made; returns
+// the row sum of the unscaled P.
+template <int NC, bool SCALED>
 __device__ __forceinline__ float exp_store(const float (&s)[NC], float c, float m_safe,
-                                           float pscale, uint32_t t_p, float& mx) {
+                                           float pscale, uint32_t t_p) {
   const uint64_t cc = f2(c, c);
   const uint64_t nm = f2(-m_safe, -m_safe);
+  const uint64_t ps = f2(pscale, pscale);
   uint64_t acc[4] = {0, 0, 0, 0};  // four packed partial sums (+0.0f bit patterns)
-  float m8[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
 #pragma unroll
   for (int ch = 0; ch < NC / 32; ++ch) {
     uint32_t pk[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int e = ch * 32 + 2 * j;
-      if (WITH_MAX && (j % 8) == 0) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = max3(m8[i], s[e + i], s[e + 8 + i]);
-      }
       const uint64_t x = f2_fma(f2(s[e], s[e + 1]), cc, nm);
       float x0, x1;
       f2_split(x, x0, x1);
-      const float p0 = ex2(x0), p1 = ex2(x1);
-      acc[j & 3] = f2_add(acc[j & 3], f2(p0, p1));
-      pk[j] = F16P ? pack_p<true>(p0 * pscale, p1 * pscale) : pack_p<false>(p0, p1);
+      const uint64_t pp = f2(ex2(x0), ex2(x1));
+      acc[j & 3] = f2_add(acc[j & 3], pp);
+      float p0, p1;
+      f2_split(SCALED ? f2_mul(pp, ps) : pp, p0, p1);
+      pk[j] = pack_bf16(p0, p1);
     }
     tmem_st16(t_p + ch * 16, pk);
   }
-  if (WITH_MAX)
-    mx = fmaxf(max3(m8[0], m8[1], m8[2]), fmaxf(max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])));
   const uint64_t acc2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
   float sa, sb;
   f2_split(acc2, sa, sb);
@@ -430,7 +285,7 @@ __device__ __forceinline__ float row_max(const float (&s)[NC]) {
 }
 
 // Exact online softmax (the recompute kernel).
-template <int NC, int D, bool F16P>
+template <int NC, int D, bool SCALED>
 __device__ __forceinline__ void softmax_tile_exact(uint32_t t_s, uint32_t t_o, bool first_tile,
                                                    bool masked, int lo_c, int hi_c, float c,
                                                    float pscale, float& m_used, float& l) {
@@ -447,8 +302,7 @@ __device__ __forceinline__ void softmax_tile_exact(uint32_t t_s, uint32_t t_o, b
     rescale = true;
   }
   const float m_safe = (m_used == -INFINITY) ? 0.0f : m_used;
-  float unused;
-  const float sum = exp_store<NC, F16P, false>(s, c, m_safe, pscale, t_s + NC / 2, unused);
+  const float sum = exp_store<NC, SCALED>(s, c, m_safe, pscale, t_s + NC / 2);
   l = l * alpha + sum;
   // The PV of the previous tile is complete (the commit that signalled this S tile
   // tracks every earlier MMA), and the PV of this tile waits for this warpgroup's P,
@@ -474,17 +328,13 @@ __device__ __forceinline__ void softmax_tile_exact(uint32_t t_s, uint32_t t_o, b
 }
 
 // Fast kernel: P = 2^(s c) against the fixed reference m = 0 (no max pass, no rescale).
-// Returns the tile's row max of s c for f16 P (computed alongside the exponentials), -inf
-// for bf16 P (whose bounds are tested on l).
-template <int NC, bool F16P>
-__device__ __forceinline__ float softmax_tile_spec(uint32_t t_s, bool masked, int lo_c, int hi_c,
-                                                   float c, float pscale, float& l) {
+template <int NC, bool SCALED>
+__device__ __forceinline__ void softmax_tile_spec(uint32_t t_s, bool masked, int lo_c, int hi_c,
+                                                  float c, float pscale, float& l) {
   float s[NC];
   load_s<NC>(t_s, masked, lo_c, hi_c, s);
-  float mx = -INFINITY;
-  l += exp_store<NC, F16P, F16P>(s, c, 0.0f, pscale, t_s + NC / 2, mx);
+  l += exp_store<NC, SCALED>(s, c, 0.0f, pscale, t_s + NC / 2);
   tmem_wait_st();
-  return F16P ? mx * c : -INFINITY;
 }
 
 // ---------------------------------------------------------------------------------
@@ -514,8 +364,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       mbar_init(&bars->q_full[q], 1);
       mbar_init(&bars->q_empty[q], 1);
       mbar_init(&bars->s_full[q], 1);
-      // one arrival per softmax warp (+ the fill checker in the BF16 variant)
-      mbar_init(&bars->p_full[q], FP8 ? 4 : 5);
+      // one arrival per softmax warp and one from the fill checker
+      mbar_init(&bars->p_full[q], 5);
       mbar_init(&bars->o_done[q], 1);
     }
     for (int s = 0; s < C::kStages; ++s) {
@@ -526,7 +376,6 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
     }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
-    bars->loader_ok = 1;
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -549,9 +398,9 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
   const int stride = gridDim.x;
 
   if (warp >= 8) {
-   // ------------------------------------------------ warpgroup 2: producer, MMA, idle
-   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<D, FP8>::kOther));
-   if (!FP8 && warp == kWarpProducer) {
+   // ------------------------------------ warpgroup 2: producer, MMA, fill checker, idle
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg<D>::kRegsOther));
+   if (warp == kWarpProducer) {
     // The whole warp walks the schedule (so every operand is warp-uniform); one elected
     // lane issues the TMA copies and the expect-tx arrivals.
     {
@@ -573,8 +422,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       for (; ok && item < total_items; item += stride, ++it_count) {
         const Item nxt = item + stride < total_items ? load_item(p, item_id(item + stride)) : it;
         const int nA = it.n_anchor_tiles();
-        const int n_tiles = it.template n_tiles<FP8>();
-        const bool sh = it.template sfx_shared<FP8>();
+        const int n_tiles = it.n_tiles();
+        const bool sh = it.sfx_shared();
         const int g = it.ag % hkv;
         for (int pos = 0; pos < n_tiles; ++pos, ++kv_seq) {
           const int slot = kv_seq % C::kStages;
@@ -646,106 +495,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         if (v_arm[s]) drain_wait(&bars->v_full[s], (v_arm[s] - 1) & 1u, dl);
       }
     }
-   } else if (FP8 && warp != kWarpMma) {
-    // ---------------------------------------------- FP8 variant: tile loaders (3 warps)
-    // All 96 threads walk the same job sequence in lockstep. Only the leader waits on an
-    // mbarrier; it publishes the outcome through shared memory across a named barrier,
-    // so an abort is seen by every loader at the same job and none is left at a barrier.
-    const int lt = (warp == kWarpProducer ? 0 : warp - 9) * 32 + lane;
-    volatile int* ok_flag = &bars->loader_ok;
-    const int gshift = __ffs(G) - 1;
-    const uint8_t* q_suf = static_cast<const uint8_t*>(p.q_suf);
-    const int64_t T_S = p.total_suffix_tokens, T_A = p.total_anchor_tokens;
-    const uint64_t keep = l2_policy_evict_last(), stream_pol = l2_policy_evict_first();
-    bool skip_pending = p.inject_skip_first_kv != 0;
-    auto acquire = [&](uint64_t* bar, uint32_t parity) -> bool {
-      if (lt == 0) *ok_flag = wait_parity(wc, bar, parity) ? 1 : 0;
-      loader_bar();
-      return *ok_flag != 0;
-    };
-    auto publish = [&](uint64_t* bar) {
-      fence_proxy_async();  // the generic-proxy stores must be visible to the tensor core
-      loader_bar();
-      if (lt == 0) mbar_arrive(bar);
-    };
-    uint32_t kv_seq = 0, it_count = 0;
-    bool ok = true;
-    int item = blockIdx.x;
-    Item it = item < total_items ? load_item(p, item_id(item)) : Item{};
-    for (; ok && item < total_items; item += stride, ++it_count) {
-      const Item nxt = item + stride < total_items ? load_item(p, item_id(item + stride)) : it;
-      const int nA = it.n_anchor_tiles();
-      const int n_tiles = it.template n_tiles<FP8>();
-      const bool sh = it.template sfx_shared<FP8>();
-      const int nk_sfx = it.nk_sfx();
-      const int g = it.ag % hkv;
-      for (int q = 0; q < 2; ++q) {
-        if (!(ok = acquire(&bars->q_empty[q], (it_count & 1u) ^ 1u))) break;
-        const int64_t t0q = it.t0 + q * tok;
-        const int valid = clamp_rows((T_S - t0q) * G, 128);
-        load_tile_bf16(smem_u32(sQ + q * C::kTileBytes),
-                       q_suf + (t0q * p.hq + g * G) * (2 * D), static_cast<int64_t>(p.hq) * 2 * D,
-                       gshift, 2 * D, 128, valid, lt, stream_pol);
-        publish(&bars->q_full[q]);
-      }
-      // Anchor tiles (e4m3): K and V of one tile alternate between two register buffers so
-      // the next job's loads are in flight while the current job is converted.
-      const uint8_t* k_src = static_cast<const uint8_t*>(p.k_anc);
-      const uint8_t* v_src = static_cast<const uint8_t*>(p.v_anc);
-      auto anc_base = [&](const uint8_t* src, int t) {
-        return src + (static_cast<int64_t>(it.a_tok0 + t * kBN) * hkv + g) * D;
-      };
-      auto anc_valid = [&](int t) { return clamp_rows(T_A - (it.a_tok0 + t * kBN), 128); };
-      const int64_t anc_stride = static_cast<int64_t>(hkv) * D;
-      uint4 kbuf[kE4m3PerThread], vbuf[kE4m3PerThread];
-      if (nA > 0) load_e4m3_regs(kbuf, anc_base(k_src, 0), anc_stride, anc_valid(0), lt, keep);
-      for (int pos = 0; ok && pos < n_tiles; ++pos, ++kv_seq) {
-        const int slot = kv_seq % C::kStages;
-        const uint32_t ph = (kv_seq / C::kStages) & 1u;
-        const uint32_t k_dst = smem_u32(sKV + slot * 2 * C::kTileBytes);
-        const uint32_t v_dst = k_dst + C::kTileBytes;
-        if (pos < nA) {
-          load_e4m3_regs(vbuf, anc_base(v_src, pos), anc_stride, anc_valid(pos), lt, keep);
-          if (!(ok = acquire(&bars->k_empty[slot], ph ^ 1u))) break;
-          store_e4m3_regs(k_dst, kbuf, lt);
-          if (skip_pending) {
-            skip_pending = false;  // fault injection: this tile is never published
-            fence_proxy_async();
-            loader_bar();
-          } else {
-            publish(&bars->k_full[slot]);
-          }
-          if (pos + 1 < nA)
-            load_e4m3_regs(kbuf, anc_base(k_src, pos + 1), anc_stride, anc_valid(pos + 1), lt,
-                           keep);
-          if (!(ok = acquire(&bars->v_empty[slot], ph ^ 1u))) break;
-          store_e4m3_regs(v_dst, vbuf, lt);
-          publish(&bars->v_full[slot]);
-        } else {
-          const int rel = pos - nA;
-          const int64_t tok0 = sh ? it.ws0 + rel * kBN : it.ws(rel & 1) + (rel >> 1) * kBN;
-          const int valid = clamp_rows(T_S - tok0, nk_sfx);
-          for (int w = 0; w < 2 && ok; ++w) {  // w = 0: K, w = 1: V
-            uint64_t* empty = w ? &bars->v_empty[slot] : &bars->k_empty[slot];
-            uint64_t* full = w ? &bars->v_full[slot] : &bars->k_full[slot];
-            if (!(ok = acquire(empty, ph ^ 1u))) break;
-            const uint8_t* src = static_cast<const uint8_t*>(w ? p.v_suf : p.k_suf);
-            load_tile_bf16(w ? v_dst : k_dst, src + (tok0 * hkv + g) * (2 * D),
-                           static_cast<int64_t>(hkv) * 2 * D, 0, 0, nk_sfx, valid, lt, stream_pol);
-            if (skip_pending) {
-              skip_pending = false;
-              fence_proxy_async();
-              loader_bar();
-            } else {
-              publish(full);
-            }
-          }
-        }
-      }
-      it = nxt;
-    }
-   } else if (!FP8 && warp == kWarpFillCheck) {
-    // ------------------------------------------------ BF16 variant: fill checker
+   } else if (warp == kWarpFillCheck) {
+    // ------------------------------------------------ fill checker
     // For every group {PV(q,k), S(q,k+1)}: wait until the V(q,k) and K(q,k+1) fills it
     // reads have landed, then add the fifth arrival on p_full[q]. Before arriving for a
     // group it waits for the previous phase of p_full[q] to complete, so it never gives
@@ -759,7 +510,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       const int nA = it.n_anchor_tiles();
       const int nS = it.n_sfx_tiles();
       const int n = nA + nS;
-      const bool sh = it.template sfx_shared<FP8>();
+      const bool sh = it.sfx_shared();
       for (int k = 0; ok && k < n; ++k) {
         for (int q = 0; ok && q < 2; ++q) {
           // shared tiles are checked once, for query tile 0 (whose group runs first)
@@ -779,14 +530,14 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           __syncwarp();
         }
       }
-      kv_base += it.template n_tiles<FP8>();
+      kv_base += it.n_tiles();
       it = nxt;
     }
    } else if (warp == kWarpMma) {
     // Whole warp walks the schedule; one elected lane issues tcgen05.mma / commit.
     {
       const bool leader = elect_one();
-      constexpr uint32_t kAB = FP8 ? 0u : 1u;  // operand type: f16 (FP8 variant) or bf16
+      constexpr uint32_t kAB = 1u;  // operand type bf16 (A and B)
       constexpr uint32_t kIdescS128 = idesc_f16(kBM, 128, kAB, 0);
       constexpr uint32_t kIdescS64 = idesc_f16(kBM, 64, kAB, 0);
       constexpr uint32_t kIdescPV = idesc_f16(kBM, D, kAB, 1);
@@ -806,13 +557,13 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         const int nS = it.n_sfx_tiles();
         const int nk_sfx = it.nk_sfx();
         const int n = nA + nS;
-        const bool sh = it.template sfx_shared<FP8>();
+        const bool sh = it.sfx_shared();
 
         // Waits (K fill, Q fill) for S(q, k) and (V fill, P ready) for PV(q, k); the MMAs
         // are issued only after every wait of the next pair of groups is done, so PV(q, k)
-        // and S(q, k + 1) go to the tensor pipe back to back. In the BF16 variant the fill
-        // checker warp folds the V(q,k) and K(q,k+1) fills into p_full[q], so after the
-        // first group of an item the MMA warp waits once per group: an mbarrier wait costs
+        // and S(q, k + 1) go to the tensor pipe back to back. The fill checker warp folds
+        // the V(q,k) and K(q,k+1) fills into p_full[q], so after the first group of an
+        // item the MMA warp waits once per group: an mbarrier wait costs
         // it a few hundred cycles while the tensor pipe reads shared memory, and the pipe's
         // queue holds only about two MMAs.
         auto wait_s = [&](int q, int k) -> bool {
@@ -825,13 +576,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           if (k == 0 && !wait_parity_warp(wc, &bars->q_full[q], it_count & 1u)) return false;
           return true;
         };
-        auto wait_pv = [&](int q, int k) -> bool {
-          const uint32_t seq = kv_base + pos_of(nA, sh, q, k);
-          const int slot = seq % C::kStages;
-          const uint32_t ph = (seq / C::kStages) & 1u;
-          const bool own = k >= nA && !sh;
-          if (FP8 && (own || q == 0) && !wait_parity_warp(wc, &bars->v_full[slot], ph))
-            return false;
+        auto wait_pv = [&](int q) -> bool {
           if (!wait_parity_warp(wc, &bars->p_full[q], p_cnt[q] & 1u)) return false;
           ++p_cnt[q];
           return true;
@@ -889,8 +634,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         }
         for (int k = 0; ok && k < n; ++k) {
           for (int q = 0; q < 2 && ok; ++q) {
-            // BF16: the fill checker's arrival on p_full covers V(q,k) and K(q,k+1)
-            ok = wait_pv(q, k) && (!FP8 || k + 1 >= n || wait_s(q, k + 1));
+            // the fill checker's arrival on p_full covers V(q,k) and K(q,k+1)
+            ok = wait_pv(q);
             if (!ok) break;
             tc_fence_after();
             if (leader) {
@@ -900,7 +645,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
             __syncwarp();
           }
         }
-        kv_base += it.template n_tiles<FP8>();
+        kv_base += it.n_tiles();
         it = nxt;
       }
       // Every MMA issued so far has completed once this barrier flips.
@@ -911,7 +656,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
    }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<D, FP8>::kSoftmax));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg<D>::kRegsSoftmax));
     const int q = warp >> 2;
     const int row = threadIdx.x & 127;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -937,7 +682,6 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       const float c_anc = FP8 ? c * __ldg(p.k_scale + it.ag) : c;
       const float v_sc = FP8 ? __ldg(p.v_scale + it.ag) : 1.0f;
       float m_used = EXACT ? -INFINITY : 0.0f, l = 0.0f;
-      float row_mx = -INFINITY;  // fast kernel: max of s c over the row's tiles
       for (int k = 0; k < n; ++k) {
         if (!(ok = wait_parity(wc, &bars->s_full[q], s_cnt & 1u))) break;
         ++s_cnt;
@@ -948,25 +692,22 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
             softmax_tile_exact<128, D, FP8>(t_s, t_o, k == 0, rem < kBN, 0, rem - 1, c_anc,
                                             v_sc, m_used, l);
           else
-            row_mx = fmaxf(row_mx, softmax_tile_spec<128, FP8>(t_s, rem < kBN, 0, rem - 1,
-                                                               c_anc, v_sc, l));
+            softmax_tile_spec<128, FP8>(t_s, rem < kBN, 0, rem - 1, c_anc, v_sc, l);
         } else {
           const int base = ws_q + (k - nA) * kBN;
           const int lo_c = vis_lo - base, hi_c = t - base;
           if (EXACT) {
             if (nk_sfx == 64)
-              softmax_tile_exact<64, D, FP8>(t_s, t_o, k == 0, true, lo_c, hi_c, c, 1.0f,
-                                             m_used, l);
+              softmax_tile_exact<64, D, false>(t_s, t_o, k == 0, true, lo_c, hi_c, c, 1.0f,
+                                               m_used, l);
             else
-              softmax_tile_exact<128, D, FP8>(t_s, t_o, k == 0, true, lo_c, hi_c, c, 1.0f,
-                                              m_used, l);
+              softmax_tile_exact<128, D, false>(t_s, t_o, k == 0, true, lo_c, hi_c, c, 1.0f,
+                                                m_used, l);
           } else {
             if (nk_sfx == 64)
-              row_mx = fmaxf(row_mx, softmax_tile_spec<64, FP8>(t_s, true, lo_c, hi_c, c,
-                                                                1.0f, l));
+              softmax_tile_spec<64, false>(t_s, true, lo_c, hi_c, c, 1.0f, l);
             else
-              row_mx = fmaxf(row_mx, softmax_tile_spec<128, FP8>(t_s, true, lo_c, hi_c, c,
-                                                                 1.0f, l));
+              softmax_tile_spec<128, false>(t_s, true, lo_c, hi_c, c, 1.0f, l);
           }
         }
         tc_fence_before();
@@ -976,8 +717,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       if (!ok) break;
       // Fast kernel: hand the item to the exact kernel if a valid row left the bounds
       // (its output rows are then written again).
-      const bool broke = FP8 ? !(row_mx >= -kSpecMaxF16 && row_mx <= kSpecMaxF16)
-                             : !(l >= kSpecSumLow && l <= kSpecSumHigh);
+      const bool broke = !(l >= kSpecSumLow && l <= kSpecSumHigh) ||
+                         (FP8 && it.la > 0 && !(fabsf(v_sc) <= kSpecScaleHigh));
       if (!EXACT && __any_sync(0xFFFFFFFFu, broke && valid) && lane == 0) {
         const int id = item_id(item);
         if (atomicExch(p.redo_flag + id, 1) == 0) p.redo_list[atomicAdd(p.redo_count, 1)] = id;
@@ -1185,6 +926,73 @@ __global__ void __launch_bounds__(256) cascade_items_kernel(const CascadeParams 
   dst[1] = r1;
 }
 
+// FP8 anchor KV staging: e4m3 codes -> bf16, exact (every e4m3 value, subnormals
+// included, is a bf16 value; the NaN codes stay NaN). Both tensors [T_A, Hkv, D] are
+// walked as one range of 16-code units: one 16-byte load and two 16-byte stores each,
+// two units per thread in flight.
+__device__ __forceinline__ uint4 ld_stream_u4(const uint8_t* p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+__device__ __forceinline__ void st_u4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+// Two f16 values of at most 4 significant bits and exponents in [-9, 8] -> bf16x2, exact
+// (f16 -> f32 is exact, and so is f32 -> bf16 for such values).
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h));
+  return pack_bf16(lo, hi);
+}
+// Four e4m3 codes (bytes 0..3 of w) -> four bf16 in two words, the lower code in the
+// lower half (memory order kept).
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& a, uint32_t& b) {
+  uint32_t h0, h1;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(h0), "=r"(h1)
+      : "r"(w));
+  a = f16x2_to_bf16x2(h0);
+  b = f16x2_to_bf16x2(h1);
+}
+__device__ __forceinline__ void convert_unit(const uint4 c, uint8_t* dst) {
+  uint32_t o[8];
+  e4m3x4_to_bf16x4(c.x, o[0], o[1]);
+  e4m3x4_to_bf16x4(c.y, o[2], o[3]);
+  e4m3x4_to_bf16x4(c.z, o[4], o[5]);
+  e4m3x4_to_bf16x4(c.w, o[6], o[7]);
+  st_u4(dst, o[0], o[1], o[2], o[3]);
+  st_u4(dst + 16, o[4], o[5], o[6], o[7]);
+}
+__global__ void __launch_bounds__(256) anchor_e4m3_to_bf16_kernel(const CascadeParams p,
+                                                                   int64_t units) {
+  const uint8_t* kc = static_cast<const uint8_t*>(p.k_anc);
+  const uint8_t* vc = static_cast<const uint8_t*>(p.v_anc);
+  uint8_t* kb = static_cast<uint8_t*>(p.k_anc_bf16);
+  uint8_t* vb = static_cast<uint8_t*>(p.v_anc_bf16);
+  const uint64_t pol = l2_policy_evict_first();
+  const int64_t total = 2 * units;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  auto src = [&](int64_t u) { return u < units ? kc + 16 * u : vc + 16 * (u - units); };
+  auto dst = [&](int64_t u) { return u < units ? kb + 32 * u : vb + 32 * (u - units); };
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < total;
+       u += 2 * step) {
+    const bool two = u + step < total;
+    const uint4 c0 = ld_stream_u4(src(u), pol);
+    const uint4 c1 = two ? ld_stream_u4(src(u + step), pol) : make_uint4(0u, 0u, 0u, 0u);
+    convert_unit(c0, dst(u));
+    if (two) convert_unit(c1, dst(u + step));
+  }
+}
+
 }  // namespace
 
 int64_t cascade_item_bound(int num_anchors, int64_t total_suffix_tokens, int hkv, int group) {
@@ -1193,7 +1001,7 @@ int64_t cascade_item_bound(int num_anchors, int64_t total_suffix_tokens, int hkv
 }
 
 CascadeWorkspace cascade_workspace_layout(int num_anchors, int64_t total_suffix_tokens,
-                                          int64_t item_bound) {
+                                          int64_t item_bound, int64_t anchor_bf16_bytes) {
   auto up = [](size_t x, size_t a) { return (x + a - 1) / a * a; };
   CascadeWorkspace w;
   w.flag = 0;
@@ -1204,7 +1012,9 @@ CascadeWorkspace cascade_workspace_layout(int num_anchors, int64_t total_suffix_
   w.items = up(w.seg + 4 * static_cast<size_t>(total_suffix_tokens), 32);
   w.redo_flag = w.items + 32 * static_cast<size_t>(item_bound);
   w.redo_list = w.redo_flag + 4 * static_cast<size_t>(item_bound);
-  w.total = up(w.redo_list + 4 * static_cast<size_t>(item_bound), 256);
+  w.k_anc_bf16 = up(w.redo_list + 4 * static_cast<size_t>(item_bound), 256);
+  w.v_anc_bf16 = up(w.k_anc_bf16 + static_cast<size_t>(anchor_bf16_bytes), 256);
+  w.total = up(w.v_anc_bf16 + static_cast<size_t>(anchor_bf16_bytes), 256);
   return w;
 }
 
@@ -1218,7 +1028,7 @@ static cudaError_t launch_attn_kernel(const CascadeParams& p, const CascadeMaps&
   // the register split must fit in what the block is launched with (else setmaxnreg.inc
   // would wait forever)
   if (static_cast<int64_t>(attr.numRegs) * kThreads <
-      256 * Regs<D, FP8>::kSoftmax + 128 * Regs<D, FP8>::kOther)
+      256 * Cfg<D>::kRegsSoftmax + 128 * Cfg<D>::kRegsOther)
     return cudaErrorInvalidConfiguration;
   e = cudaFuncSetAttribute(cascade_attn_kernel<D, FP8, EXACT>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -1255,9 +1065,18 @@ cudaError_t launch_cascade(const CascadeParams& p, const CascadeMaps& maps, int 
     cascade_items_kernel<<<(p.item_bound + 255) / 256, 256, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (fp8) return launch_attn_d<128, true>(p, maps, num_sms, stream);
-  if (head_dim == 128) return launch_attn_d<128, false>(p, maps, num_sms, stream);
-  return launch_attn_d<64, false>(p, maps, num_sms, stream);
+  if (fp8 && p.total_anchor_tokens > 0) {
+    const int64_t units = p.total_anchor_tokens * p.hkv * head_dim / 16;
+    const int blocks = static_cast<int>(
+        std::min<int64_t>((units + 255) / 256, static_cast<int64_t>(num_sms) * 8));
+    anchor_e4m3_to_bf16_kernel<<<blocks, 256, 0, stream>>>(p, units);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (head_dim == 128)
+    return fp8 ? launch_attn_d<128, true>(p, maps, num_sms, stream)
+               : launch_attn_d<128, false>(p, maps, num_sms, stream);
+  return fp8 ? launch_attn_d<64, true>(p, maps, num_sms, stream)
+             : launch_attn_d<64, false>(p, maps, num_sms, stream);
 }
 
 }  // namespace quail

@@ -49,8 +49,8 @@ struct CascadeParams {
   const int32_t* suffix_offsets;
   const float* k_scale;
   const float* v_scale;
-  const void* q_suf;         // raw pointers (the FP8 variant loads tiles without TMA)
-  const void* k_anc;
+  const void* q_suf;
+  const void* k_anc;         // bf16, or e4m3 codes with FP8 anchor KV
   const void* v_anc;
   const void* k_suf;
   const void* v_suf;
@@ -65,6 +65,8 @@ struct CascadeParams {
   int32_t* redo_count;       // items the speculative kernel handed to the exact one
   int32_t* redo_flag;        // [item_bound] nonzero: item is in redo_list
   int32_t* redo_list;        // [item_bound] item indices, redo_count of them valid
+  void* k_anc_bf16;          // FP8 anchor KV: [T_A, Hkv, D] bf16 copies of the codes
+  void* v_anc_bf16;
   unsigned* err_word;
   uint64_t timeout_ns;
   int inject_skip_first_kv;
@@ -72,10 +74,13 @@ struct CascadeParams {
 
 // Byte offsets of the workspace regions; `total` is the size to allocate.
 struct CascadeWorkspace {
-  size_t flag, redo_count, prefix, order, seg, items, redo_flag, redo_list, total;
+  size_t flag, redo_count, prefix, order, seg, items, redo_flag, redo_list, k_anc_bf16,
+      v_anc_bf16, total;
 };
+// anchor_bf16_bytes: T_A * Hkv * D * 2 with FP8 anchor KV (each of the two staged
+// copies), else 0.
 CascadeWorkspace cascade_workspace_layout(int num_anchors, int64_t total_suffix_tokens,
-                                          int64_t item_bound);
+                                          int64_t item_bound, int64_t anchor_bf16_bytes);
 int64_t cascade_item_bound(int num_anchors, int64_t total_suffix_tokens, int hkv, int group);
 
 // Tensor maps over q_suf, k/v anchor and k/v suffix (bf16, 3-D: d, head, token).

@@ -6,8 +6,9 @@
 // host framework whose plugin interface only hands over input and output buffers, or
 // code on a latency path where an allocation (which can synchronise the device) is not
 // allowed. For them the scratch that the cascade kernels need (offset-check flag, anchor
-// order, work-item prefix, per-token suffix starts and one record per work item) lives in
-// a file-scope device array of fixed size instead of a caller workspace.
+// order, work-item prefix, per-token suffix starts, one record per work item and, with FP8
+// anchor KV, the anchors widened to bf16) lives in a file-scope device array of fixed size
+// instead of a caller workspace.
 //
 // Cost and limits:
 //   - Every GPU on which the library's kernels are loaded holds kScratchBytes (64 MiB)

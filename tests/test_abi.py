@@ -45,6 +45,11 @@ def test_workspace_size():
     assert q.cascade_workspace_size(d) >= (2 * 8 + 1) * 4
     assert q.cascade_workspace_size(d) % 256 == 0
     assert q.lib.quail_cascade_workspace_size(None) == 0
+    # FP8 anchor KV: the workspace also holds the anchor codes widened to bf16, two
+    # [T_A, Hkv, d] copies (each placed on a 256-byte boundary)
+    d8 = q.make_desc(8, 33152, 8192, 530000, 1024, 24, 32, 8, 128, kv_fp8=True)
+    extra = q.cascade_workspace_size(d8) - q.cascade_workspace_size(d)
+    assert 4 * 8192 * 8 * 128 <= extra <= 4 * 8192 * 8 * 128 + 512
 
 
 def _call_attn(desc, fake=0x10000, ws_bytes=1 << 20, **over):
@@ -94,8 +99,12 @@ def test_cascade_rejects_bad_pointers():
     assert _call_attn(d, ks=0x10000) == q.QUAIL_ERR_INVALID_ARG           # scales with bf16
     fp8 = _good_desc(kv_fp8=True)
     assert _call_attn(fp8) == q.QUAIL_ERR_INVALID_ARG                     # fp8 without scales
-    assert _call_attn(_good_desc(kv_fp8=True, head_dim=64), ks=0x10000, vs=0x10000) == \
+    assert _call_attn(_good_desc(kv_fp8=True, head_dim=96), ks=0x10000, vs=0x10000) == \
         q.QUAIL_ERR_UNSUPPORTED
+    # FP8 needs room for the staged bf16 anchors: the BF16-sized workspace is too small
+    bf16_bytes = q.cascade_workspace_size(_good_desc())
+    assert _call_attn(fp8, ks=0x10000, vs=0x10000, ws_bytes=bf16_bytes) == \
+        q.QUAIL_ERR_INVALID_ARG
 
 
 def test_head_rejects_bad_arguments():

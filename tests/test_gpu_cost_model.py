@@ -1,6 +1,7 @@
-"""The cost model against live kernel times on the GPU: a reduced join plan and a reduced
-causal-prefill plan, each timed through the C ABI with CUDA events; the model must land
-within 20 % (it was calibrated on other plans' traces and times)."""
+"""The cost model against live kernel times on the GPU: a reduced join plan, a reduced
+causal-prefill plan and a reduced FP8 long-anchor plan, each timed through the C ABI with
+CUDA events; the model must land within 20 % (it was calibrated on other plans' traces
+and times)."""
 import dataclasses
 
 import pytest
@@ -29,6 +30,7 @@ def _time(fn, reps=5):
 @pytest.mark.parametrize("name,changes", [
     ("join", {"suffixes_per_anchor": 1024}),
     ("prefill", {"num_anchors": 16}),
+    ("fp8_long", {"suffixes_per_anchor": 128}),
 ])
 def test_model_within_20_percent(name, changes):
     import prefill_only_cascade_gb300 as q
@@ -36,17 +38,29 @@ def test_model_within_20_percent(name, changes):
     lay = workloads.make_layout(cfg)
     t = workloads.make_attention_inputs(cfg, lay, "cuda")
     heads = (cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim)
+    scales = (None, None)
+    if cfg.kv_fp8:
+        sc = []
+        for name_ in ("k_anc", "v_anc"):
+            codes = torch.empty(t[name_].shape, dtype=torch.uint8, device="cuda")
+            scale = torch.empty(lay.num_anchors, cfg.num_kv_heads, dtype=torch.float32,
+                                device="cuda")
+            q.quantize_kv_fp8(t[name_], t["anchor_offsets"], codes, scale)
+            t[name_] = codes
+            sc.append(scale)
+        scales = tuple(sc)
     desc = q.make_desc(lay.num_anchors, lay.num_suffixes, lay.total_anchor_tokens,
-                       lay.total_suffix_tokens, lay.max_anchor_len, lay.max_suffix_len, *heads)
+                       lay.total_suffix_tokens, lay.max_anchor_len, lay.max_suffix_len, *heads,
+                       0.0, cfg.kv_fp8)
     ws = torch.empty(q.cascade_workspace_size(desc), dtype=torch.uint8, device="cuda")
     out = torch.empty(lay.total_suffix_tokens, cfg.num_q_heads, cfg.head_dim,
                       dtype=torch.bfloat16, device="cuda")
     run = lambda: q.cascade_attn(desc, t["q_suf"], t["k_anc"], t["v_anc"], t["k_suf"],
                                  t["v_suf"], t["anchor_offsets"], t["anchor_suffix_ptr"],
-                                 t["suffix_offsets"], out, None, ws)
+                                 t["suffix_offsets"], out, None, ws, *scales)
     measured = _time(run)
     assert q.get_device_error() == q.QUAIL_OK
     model = cm.kernel_seconds(lay.anchor_offsets, lay.anchor_suffix_ptr, lay.suffix_offsets,
-                              *heads, cm.default_hardware())["seconds"]
+                              *heads, cm.default_hardware(), fp8=cfg.kv_fp8)["seconds"]
     print(name, "measured %.3f ms, model %.3f ms" % (measured * 1e3, model * 1e3))
     assert abs(model / measured - 1) < 0.20

@@ -3,8 +3,8 @@
 Anchor K/V are drawn in bf16 and quantised per (anchor, KV head) by
 quail_quantize_kv_fp8; the oracle quantises the same bf16 values itself (bit-exact
 agreement of the codes is checked too) and attends over the dequantised values
-decode(code) * scale. Bound: relative L2 <= 3e-2 (plus the bf16 max-abs and LSE bounds,
-which this path also meets)."""
+decode(code) * scale. Bounds: relative L2 <= 3e-2, the LSE bound of the bf16 path, and
+max-abs <= 2e-2 + 2^-9 x the largest |V| (parity_util.fp8_max_abs)."""
 import zlib
 
 import numpy as np
@@ -14,7 +14,7 @@ import torch
 import oracle
 import workloads
 from oracle.fp8 import dequantize_kv_fp8
-from parity_util import FP8_REL_L2, check_full, check_sampled, np64, run_cascade
+from parity_util import FP8_REL_L2, check_full, check_sampled, fp8_max_abs, np64, run_cascade
 
 pytestmark = pytest.mark.gpu
 
@@ -43,17 +43,20 @@ FP8_CASES = {
     "gqa8": ([128, 129, 1], [5, 5, 5], (1, 50), (16, 2)),
     "gqa16": ([64, 383], [9, 4], (1, 24), (16, 1)),
     "no_anchor_keys": ([0, 0], [3, 2], [5, 1, 17, 33, 2], (8, 2)),
+    "d64_gqa4": ([0, 5, 130, 300, 256], [3, 0, 7, 2, 4], (0, 40), (8, 2), 64),
+    "d64_gqa8_long": ([700, 129], [4, 6], (1, 90), (16, 2), 64),
 }
 
 
 @pytest.mark.parametrize("name", sorted(FP8_CASES))
 def test_fp8_edge_layouts_every_element(name):
-    anchors, counts, lens, (hq, hkv) = FP8_CASES[name]
+    anchors, counts, lens, (hq, hkv), *rest = FP8_CASES[name]
+    d = rest[0] if rest else 128
     rng = np.random.default_rng(zlib.crc32(name.encode()))
     if isinstance(lens, tuple):
         lens = rng.integers(lens[0], lens[1] + 1, size=sum(counts))
     lay = workloads.layout_from_lengths(anchors, counts, lens)
-    cfg = workloads.AttnConfig("fp8case", lay.num_anchors, (0, 0), 0, (0, 0), hq, hkv, 128,
+    cfg = workloads.AttnConfig("fp8case", lay.num_anchors, (0, 0), 0, (0, 0), hq, hkv, d,
                                True, 31)
     t = workloads.make_attention_inputs(cfg, lay, "cuda")
     qz = _quantise(t, lay, hkv)
@@ -62,9 +65,10 @@ def test_fp8_edge_layouts_every_element(name):
     np.testing.assert_array_equal(qz["k_anc"][0].cpu().numpy(), kc)
     np.testing.assert_array_equal(qz["v_anc"][1].cpu().numpy(), vs)
     t8 = dict(t, k_anc=qz["k_anc"][0], v_anc=qz["v_anc"][0])
-    out, lse = run_cascade((hq, hkv, 128), lay, t8, kv_fp8=True, k_scale=qz["k_anc"][1],
+    out, lse = run_cascade((hq, hkv, d), lay, t8, kv_fp8=True, k_scale=qz["k_anc"][1],
                            v_scale=qz["v_anc"][1])
-    figs = check_full((hq, hkv, 128), lay, t, out, lse, kv=(kd, vd), rel_bound=FP8_REL_L2)
+    figs = check_full((hq, hkv, d), lay, t, out, lse, kv=(kd, vd), rel_bound=FP8_REL_L2,
+                      max_abs=fp8_max_abs(t["v_anc"]))
     print(name, figs)
 
 
@@ -94,7 +98,8 @@ def test_fp8_full_size_workload_sampled_rows():
             cache[a] = tuple(pair)
         return cache[a]
 
-    figs = check_sampled(heads, lay, t, out, lse, ids, kv_override=kv_for, rel_bound=FP8_REL_L2)
+    figs = check_sampled(heads, lay, t, out, lse, ids, kv_override=kv_for, rel_bound=FP8_REL_L2,
+                         max_abs=fp8_max_abs(t["v_anc"]))
     print("fp8_long", figs)
     del t, t8, out, lse, qz
     torch.cuda.empty_cache()
@@ -125,4 +130,5 @@ def test_fp8_missing_tile_times_out_cleanly():
                              v_scale=qz["v_anc"][1])
     kd = _oracle_kv(t, lay, "k_anc")[2]
     vd = _oracle_kv(t, lay, "v_anc")[2]
-    check_full((8, 2, 128), lay, t, out2, lse2, kv=(kd, vd), rel_bound=FP8_REL_L2)
+    check_full((8, 2, 128), lay, t, out2, lse2, kv=(kd, vd), rel_bound=FP8_REL_L2,
+               max_abs=fp8_max_abs(t["v_anc"]))

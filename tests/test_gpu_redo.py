@@ -1,10 +1,11 @@
 """GPU parity of the exact recompute path.
 
 The fast cascade kernel computes P = 2^(s c) with no max subtracted and lists a work item
-for the exact kernel when a valid row's max of s c leaves its bounds (bf16 P: [-64, 32],
-FP8 variant: [-8, 8], log2 units). Seeded inputs with large or very negative logits force
-that path, for all items or only some; every output element is compared with the float64
-oracle, and the workspace's redo counter shows the exact kernel did run."""
+for the exact kernel when a valid row's sum of P leaves [2^-64, 2^32] (with FP8 anchor KV
+also when the anchor's V scale is above 2^64). Seeded inputs with large or very negative
+logits, or a huge V scale, force that path, for all items or only some; every output
+element is compared with the float64 oracle, and the workspace's redo counter shows the
+exact kernel did run."""
 import zlib
 
 import numpy as np
@@ -14,7 +15,8 @@ import torch
 import oracle
 import workloads
 from oracle.fp8 import dequantize_kv_fp8
-from parity_util import FP8_REL_L2, check_full, np64, redo_count, run_cascade
+from parity_util import (FP8_REL_L2, check_full, compare, fp8_max_abs, np64, redo_count,
+                         run_cascade)
 
 pytestmark = pytest.mark.gpu
 
@@ -76,24 +78,53 @@ def test_very_negative_scores_recomputed():
     check_full((8, 2, 128), lay, t, out, lse)
 
 
-def test_fp8_large_logits_recomputed():
+def _fp8_run(lay, t, heads):
     import prefill_only_cascade_gb300 as q
-    lay, t = _case([513, 40], [6, 9], (1, 96), (32, 8, 128), 14)
-    # s c spread ~11 with queries x 8: above the f16-P bound of 8
-    t["q_suf"] = (t["q_suf"].float() * 8).to(torch.bfloat16)
+    hkv = heads[1]
     qz = {}
     for name in ("k_anc", "v_anc"):
         codes = torch.empty(t[name].shape, dtype=torch.uint8, device="cuda")
-        scale = torch.empty(lay.num_anchors, 8, dtype=torch.float32, device="cuda")
+        scale = torch.empty(lay.num_anchors, hkv, dtype=torch.float32, device="cuda")
         q.quantize_kv_fp8(t[name], t["anchor_offsets"], codes, scale)
         qz[name] = (codes, scale)
     t8 = dict(t, k_anc=qz["k_anc"][0], v_anc=qz["v_anc"][0])
-    out, lse, ws = run_cascade((32, 8, 128), lay, t8, kv_fp8=True, k_scale=qz["k_anc"][1],
-                               v_scale=qz["v_anc"][1], keep_ws=True)
-    assert redo_count(ws) > 0
+    return run_cascade(heads, lay, t8, kv_fp8=True, k_scale=qz["k_anc"][1],
+                       v_scale=qz["v_anc"][1], keep_ws=True)
+
+
+def _fp8_oracle_kv(t, lay):
     kv = []
     for name in ("k_anc", "v_anc"):
         codes, scales = oracle.quantize_kv_fp8(np64(t[name]).astype(np.float32),
                                                lay.anchor_offsets)
         kv.append(dequantize_kv_fp8(codes, scales, lay.anchor_offsets))
-    check_full((32, 8, 128), lay, t, out, lse, kv=tuple(kv), rel_bound=FP8_REL_L2)
+    return tuple(kv)
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_fp8_large_logits_recomputed(d):
+    lay, t = _case([513, 40], [6, 9], (1, 96), (32, 8, d), 14)
+    # queries x 24: s c has a spread of ~35 (log2 units), above the bound of 32
+    t["q_suf"] = (t["q_suf"].float() * 24).to(torch.bfloat16)
+    out, lse, ws = _fp8_run(lay, t, (32, 8, d))
+    assert redo_count(ws) > 0
+    check_full((32, 8, d), lay, t, out, lse, kv=_fp8_oracle_kv(t, lay), rel_bound=FP8_REL_L2,
+               max_abs=fp8_max_abs(t["v_anc"]))
+
+
+def test_fp8_huge_v_scale_recomputed():
+    # anchor and suffix V x 2^72 (exact in bf16; the codes are unchanged and v_scale grows
+    # by 2^72, past 2^64): every item with anchor keys goes to the exact kernel, and the
+    # output is 2^72 times the output for the unscaled V
+    lay, t = _case([300, 0, 200], [4, 2, 3], (1, 40), (8, 2, 128), 15)
+    big = dict(t)
+    for name in ("v_anc", "v_suf"):
+        big[name] = (t[name].float() * 2.0 ** 72).to(torch.bfloat16)
+    out, lse, ws = _fp8_run(lay, big, (8, 2, 128))
+    assert redo_count(ws) > 0
+    k_anc, v_anc = _fp8_oracle_kv(t, lay)
+    ref_out, ref_lse = oracle.cascade_attention(
+        np64(t["q_suf"]), k_anc, v_anc, np64(t["k_suf"]), np64(t["v_suf"]),
+        lay.anchor_offsets, lay.anchor_suffix_ptr, lay.suffix_offsets, 1.0 / np.sqrt(128))
+    compare(np64(out) / 2.0 ** 72, np64(lse), ref_out, ref_lse, rel_bound=FP8_REL_L2,
+            max_abs=fp8_max_abs(t["v_anc"]))
