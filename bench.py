@@ -576,7 +576,8 @@ def run_prefill(args):
                        "kv_heads": hkv, "head_dim": d, "l2": "inputs larger than L2 (no flush)"},
             "roofline": {"bound": "tensor", "achieved": round(tflops, 2),
                          "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": round(tflops / pk["bf16_tflops"], 4), "traffic": None,
+                         "frac": round(tflops / pk["bf16_tflops"], 4),
+                         "traffic": traffic_from_profile("cascade.cu", "cascade_attn_prefill.md"),
                          "peak_source": f"bf16_tflops (burst) of {src}",
                          "kernel": "cascade_attn_kernel (anchors of length 0), one call",
                          "algorithmic_flops_per_launch": flops},

@@ -88,8 +88,9 @@ def sol_seconds(flops: float, bytes_: float, hw: Hardware = Hardware()) -> float
 def work_items(anchor_offsets, anchor_suffix_ptr, suffix_offsets, hq: int, hkv: int) -> dict:
     """The work items the kernel's schedule builds, in its order: anchors by decreasing
     anchor-tile count (ties in index order), then per anchor KV head g major and query-tile
-    pairs minor. Each item: anchor length, and for its two query tiles the suffix-key window
-    start (the first token of the suffix that holds the tile's first token) and end."""
+    pairs minor. Each item: anchor length, and for its two query tiles the first token,
+    the suffix-key window start (the first token of the suffix that holds the tile's first
+    token), the end, and the start of the suffix that holds its last token."""
     ao = np.asarray(anchor_offsets, dtype=np.int64)
     asp = np.asarray(anchor_suffix_ptr, dtype=np.int64)
     so = np.asarray(suffix_offsets, dtype=np.int64)
@@ -99,7 +100,7 @@ def work_items(anchor_offsets, anchor_suffix_ptr, suffix_offsets, hq: int, hkv: 
     seg = np.repeat(so[:-1], so[1:] - so[:-1])   # suffix start of every token
     tiles = (la + KEYS - 1) // KEYS
     order = np.argsort(-tiles, kind="stable")
-    cols = {k: [] for k in ("la", "ws0", "ws1", "tend0", "tend1")}
+    cols = {k: [] for k in ("la", "ws0", "ws1", "tend0", "tend1", "t0", "t1", "sl0", "sl1")}
     for a in order:
         s_begin, s_end = int(so[asp[a]]), int(so[asp[a + 1]])
         ntok = s_end - s_begin
@@ -113,12 +114,18 @@ def work_items(anchor_offsets, anchor_suffix_ptr, suffix_offsets, hq: int, hkv: 
         tend1 = np.where(has1, np.minimum(t1 + tok, s_end), t1)
         ws0 = seg[t0]
         ws1 = np.where(has1, seg[np.minimum(t1, s_end - 1)], t1)
+        sl0 = seg[tend0 - 1]
+        sl1 = np.where(has1, seg[np.minimum(tend1, s_end) - 1], t1)
         for _ in range(hkv):
             cols["la"].append(np.full(pairs, la[a]))
             cols["ws0"].append(ws0)
             cols["ws1"].append(ws1)
             cols["tend0"].append(tend0)
             cols["tend1"].append(tend1)
+            cols["t0"].append(t0)
+            cols["t1"].append(t1)
+            cols["sl0"].append(sl0)
+            cols["sl1"].append(sl1)
     return {k: (np.concatenate(v) if v else np.zeros(0, np.int64)) for k, v in cols.items()}
 
 
@@ -142,12 +149,26 @@ def item_mma_cycles(items: dict, d: int, hw: Hardware = Hardware()) -> np.ndarra
 
 
 def masked_tiles(items: dict) -> np.ndarray:
-    """Masked KV tiles of each item, counted per query tile: every suffix tile, and the
-    last anchor tile when the anchor length is not a multiple of 128."""
+    """Masked KV tiles of each item, counted per query tile: the last anchor tile when the
+    anchor length is not a multiple of 128, and every suffix tile that some row of the
+    query tile does not see whole (a row sees keys from the start of its suffix up to
+    itself; the kernel skips the mask per warp, this counts per query tile)."""
     la = items["la"]
     window = np.maximum(items["tend0"] - items["ws0"], items["tend1"] - items["ws1"])
     n_sfx = (window + KEYS - 1) // KEYS
-    return 2 * (n_sfx + (la % KEYS != 0))
+    nk = np.where((n_sfx == 1) & (window <= 64), 64, KEYS)
+    count = 2 * (la % KEYS != 0).astype(np.int64)
+    for q in (0, 1):
+        ws, t0, sl = items[f"ws{q}"], items[f"t{q}"], items[f"sl{q}"]
+        # tile i covers keys ws + i*128 .. + nk - 1; whole for every row iff
+        # its last key <= t0 (first row's token) and sl <= its first key
+        i_max = int(n_sfx.max()) if n_sfx.size else 0
+        for i in range(i_max):
+            base = ws + i * KEYS
+            live = i < n_sfx
+            whole = (base + nk - 1 <= t0) & (sl <= base)
+            count += (live & ~whole).astype(np.int64)
+    return count
 
 
 def staging_seconds(anchor_offsets, hkv: int, d: int, hw: Hardware = Hardware()) -> float:

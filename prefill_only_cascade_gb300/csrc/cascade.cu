@@ -696,18 +696,21 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         } else {
           const int base = ws_q + (k - nA) * kBN;
           const int lo_c = vis_lo - base, hi_c = t - base;
+          // the column mask is skipped when every row of the warp sees the whole tile
+          // (the tiles below the diagonal of a long suffix)
+          const bool mk = __any_sync(0xFFFFFFFFu, lo_c > 0 || hi_c < nk_sfx - 1);
           if (EXACT) {
             if (nk_sfx == 64)
-              softmax_tile_exact<64, D, false>(t_s, t_o, k == 0, true, lo_c, hi_c, c, 1.0f,
+              softmax_tile_exact<64, D, false>(t_s, t_o, k == 0, mk, lo_c, hi_c, c, 1.0f,
                                                m_used, l);
             else
-              softmax_tile_exact<128, D, false>(t_s, t_o, k == 0, true, lo_c, hi_c, c, 1.0f,
+              softmax_tile_exact<128, D, false>(t_s, t_o, k == 0, mk, lo_c, hi_c, c, 1.0f,
                                                 m_used, l);
           } else {
             if (nk_sfx == 64)
-              softmax_tile_spec<64, false>(t_s, true, lo_c, hi_c, c, 1.0f, l);
+              softmax_tile_spec<64, false>(t_s, mk, lo_c, hi_c, c, 1.0f, l);
             else
-              softmax_tile_spec<128, false>(t_s, true, lo_c, hi_c, c, 1.0f, l);
+              softmax_tile_spec<128, false>(t_s, mk, lo_c, hi_c, c, 1.0f, l);
           }
         }
         tc_fence_before();

@@ -56,10 +56,28 @@ def test_item_mma_cycles_by_hand():
     # 256 anchor keys (2 full tiles) and two 32-token query tiles whose windows are 32 keys:
     # per query tile 2 x (S 8 x 96 + PV 8 x 72) + one 64-key suffix tile (8 x 68 + 4 x 72)
     items = {"la": np.array([256]), "ws0": np.array([0]), "ws1": np.array([32]),
-             "tend0": np.array([32]), "tend1": np.array([64])}
+             "tend0": np.array([32]), "tend1": np.array([64]), "t0": np.array([0]),
+             "t1": np.array([32]), "sl0": np.array([0]), "sl1": np.array([32])}
     per_q = 2 * (8 * 96 + 8 * 72) + (8 * 68 + 4 * 72)
     assert cm.item_mma_cycles(items, 128, hw)[0] == 2 * per_q
     assert cm.masked_tiles(items)[0] == 2 * 1        # the suffix tile; anchor tiles full
+
+
+def test_masked_tiles_of_a_long_suffix():
+    # one sequence of 1,024 tokens with no anchor (the causal-prefill shape), G = 4: a
+    # query tile of 32 tokens starting at token t0 sees tiles below floor((t0 + 1) / 128)
+    # whole; only the diagonal tile (and, for the item's shorter tile, the tile beyond
+    # its own window) needs the mask
+    ao, asp, so = _layout([0], [1], [1024])
+    items = cm.work_items(ao, asp, so, 32, 8)
+    m = cm.masked_tiles(items)
+    assert m.size == 8 * 16
+    for k in range(16):  # item k: query tiles at tokens 64k and 64k + 32
+        t0, t1 = 64 * k, 64 * k + 32
+        n = (t1 + 32 + 127) // 128                   # suffix tiles of the item
+        whole0 = sum(1 for i in range(n) if 128 * i + 127 <= t0)
+        whole1 = sum(1 for i in range(n) if 128 * i + 127 <= t1)
+        assert m[k] == 2 * n - whole0 - whole1
 
 
 def test_model_time_grows_with_work_and_beats_nothing_below_sol():
