@@ -425,6 +425,10 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         const int n_tiles = it.n_tiles();
         const bool sh = it.sfx_shared();
         const int g = it.ag % hkv;
+        // Suffix tiles of a window longer than one tile (a long sequence) are re-read by
+        // every later query tile of that sequence: keep them in L2 like anchor tiles.
+        // Short windows (join) are read by one or two items: stream them.
+        const uint64_t sfx_pol = it.n_sfx_tiles() > 1 ? keep : stream_pol;
         for (int pos = 0; pos < n_tiles; ++pos, ++kv_seq) {
           const int slot = kv_seq % C::kStages;
           const uint32_t ph = (kv_seq / C::kStages) & 1u;
@@ -442,7 +446,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
             mk = &maps.k_suf;
             mv = &maps.v_suf;
             row = sh ? it.ws0 + rel * kBN : it.ws(rel & 1) + (rel >> 1) * kBN;
-            pol = stream_pol;
+            pol = sfx_pol;
           }
           uint8_t* k_dst = sKV + slot * 2 * C::kTileBytes;
           uint8_t* v_dst = k_dst + C::kTileBytes;
