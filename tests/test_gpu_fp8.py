@@ -132,3 +132,37 @@ def test_fp8_missing_tile_times_out_cleanly():
     vd = _oracle_kv(t, lay, "v_anc")[2]
     check_full((8, 2, 128), lay, t, out2, lse2, kv=(kd, vd), rel_bound=FP8_REL_L2,
                max_abs=fp8_max_abs(t["v_anc"]))
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_fp8_staged_anchor_copy_is_exact_for_every_code(d):
+    """The attention reads the anchor codes widened to bf16 by the staging kernel: check
+    that copy bit for bit against the oracle's decode, for all 256 codes (signed zeros,
+    subnormals, the largest finite values and the two NaN codes). White-box: the two
+    staged copies are the last 2 x T_A x Hkv x d x 2 bytes of the workspace (K, then V)."""
+    hkv, hq = 2, 8
+    lay = workloads.layout_from_lengths([512, 256], [1, 2], [8, 3, 5])
+    cfg = workloads.AttnConfig("fp8stage", 2, (0, 0), 0, (0, 0), hq, hkv, d, True, 41)
+    t = workloads.make_attention_inputs(cfg, lay, "cuda")
+    T_A = lay.total_anchor_tokens
+    n = T_A * hkv * d
+    k_codes = (torch.arange(n, dtype=torch.int64) % 256).to(torch.uint8).reshape(T_A, hkv, d)
+    g = torch.Generator().manual_seed(41)
+    v_codes = k_codes.flatten()[torch.randperm(n, generator=g)].reshape(T_A, hkv, d)
+    ones = torch.ones(2, hkv, dtype=torch.float32, device="cuda")
+    t8 = dict(t, k_anc=k_codes.cuda(), v_anc=v_codes.cuda())
+    _, _, ws = run_cascade((hq, hkv, d), lay, t8, kv_fp8=True, k_scale=ones, v_scale=ones,
+                           keep_ws=True)
+    nbytes = n * 2
+    staged = {"k": ws[ws.numel() - 2 * nbytes: ws.numel() - nbytes],
+              "v": ws[ws.numel() - nbytes:]}
+    for name, codes in (("k", k_codes), ("v", v_codes)):
+        got = staged[name].view(torch.bfloat16).float().cpu().numpy().reshape(-1)
+        ref = oracle.e4m3_decode(codes.numpy().reshape(-1))
+        nan = np.isnan(ref)
+        assert nan.sum() == 2 * n // 256                 # codes 0x7F and 0xFF
+        np.testing.assert_array_equal(np.isnan(got), nan)
+        np.testing.assert_array_equal(got[~nan], ref[~nan].astype(np.float32))
+        # signed zeros: code 0x80 is -0
+        neg_zero = codes.numpy().reshape(-1) == 0x80
+        assert np.signbit(got[neg_zero]).all() and not np.signbit(got[codes.numpy().reshape(-1) == 0]).any()
