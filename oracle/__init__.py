@@ -29,6 +29,10 @@ kv_plan.py: the anchor-KV cache plan of a known query plan (LRU, furthest-next-u
 and the exhaustive minimum regret); pins in tests/test_oracle_kv_plan.py (a hand-worked
 plan, furthest-next-use equal to the exhaustive minimum for equal sizes, bounds).
 
+shard.py: sharding one batch over ranks by anchor (visible-pair work per anchor,
+longest-processing-time-first, the exhaustive optimum); pins in tests/test_oracle_shard.py
+(pair counts from the mask, Graham's bound against the optimum, a textbook worst case).
+
 Pins (tests/test_oracle.py): brute-force loops, the cascade-merge = monolithic identity,
 closed forms, a library SDPA with an explicit mask, RMSNorm closed forms, all 256 E4M3
 codes against the OCP formula and against torch's float8_e4m3fn. No function here is
