@@ -167,6 +167,30 @@ quail_status quail_kv_plan(int32_t num_anchors, const int64_t* anchor_tokens,
                            int64_t capacity_tokens, int32_t policy, uint8_t* hit,
                            quail_kv_plan_stats* stats);
 
+/*
+ * Sharding one batch over ranks by anchor ([P1] "Como funciona", cascade-attention
+ * bullet: a suffix attends only to its own anchor and to itself, so an anchor with its
+ * suffixes is an independent unit and ranks exchange no data). HOST call on HOST memory
+ * (no GPU work).
+ *
+ *   anchor_offsets [A+1], anchor_suffix_ptr [A+1] (anchor_suffix_ptr[0] == 0),
+ *   suffix_offsets [S+1] (S = anchor_suffix_ptr[A]): int32, as for quail_cascade_attn;
+ *                  only differences are used, each must be >= 0
+ *   num_ranks      >= 1
+ *   rank_of_anchor [A] out: the rank that computes anchor a and all its suffixes
+ *   rank_pairs     [num_ranks] out (may be NULL): visible (query, key) pairs per rank
+ * Work of an anchor = sum over its suffixes of l_s L_a + l_s (l_s + 1) / 2 (attention
+ * FLOPs / (4 d Hq)). Assignment: longest processing time first - anchors by decreasing
+ * work (ties: lower index), each to the least-loaded rank (ties: lower rank); its largest
+ * rank load is at most (4/3 - 1/(3 num_ranks)) times the best possible.
+ * Errors: QUAIL_ERR_INVALID_ARG for negative counts or lengths, num_ranks < 1, NULL
+ * arrays, or anchor_suffix_ptr[0] != 0.
+ */
+quail_status quail_shard_anchors(int32_t num_anchors, const int32_t* anchor_offsets,
+                                 const int32_t* anchor_suffix_ptr,
+                                 const int32_t* suffix_offsets, int32_t num_ranks,
+                                 int32_t* rank_of_anchor, int64_t* rank_pairs);
+
 /* Size of the library's fixed device scratch array used by quail_cascade_attn_noalloc. */
 #define QUAIL_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 

@@ -32,7 +32,7 @@ EXPORTED_SYMBOLS = (
     "quail_quantize_kv_fp8", "quail_status_string", "quail_get_device_error",
     "quail_set_wait_timeout_ns", "quail_debug_inject", "quail_version",
     "quail_cascade_attn_noalloc", "quail_causal_prefill_attn",
-    "quail_causal_prefill_workspace_size", "quail_kv_plan",
+    "quail_causal_prefill_workspace_size", "quail_kv_plan", "quail_shard_anchors",
 )
 
 
@@ -106,6 +106,8 @@ def _load():
     lib.quail_causal_prefill_workspace_size.restype = ctypes.c_size_t
     lib.quail_kv_plan.argtypes = [i32, vp, i64, vp, i64, i32, vp, ctypes.POINTER(KvPlanStats)]
     lib.quail_kv_plan.restype = ctypes.c_int
+    lib.quail_shard_anchors.argtypes = [i32, vp, vp, vp, i32, vp, vp]
+    lib.quail_shard_anchors.restype = ctypes.c_int
     return lib
 
 
@@ -208,6 +210,47 @@ def kv_plan(access_anchor, anchor_tokens, capacity_tokens, policy=KV_FURTHEST_NE
                              ctypes.byref(st))
     _check(code, "quail_kv_plan")
     return hit, {f: getattr(st, f) for f, _ in KvPlanStats._fields_}
+
+
+def shard_anchors(anchor_offsets, anchor_suffix_ptr, suffix_offsets, num_ranks):
+    """quail_shard_anchors on host arrays: returns (rank of each anchor int32 [A], visible
+    (query, key) pairs per rank int64 [num_ranks])."""
+    import numpy as np
+    ao = np.ascontiguousarray(anchor_offsets, dtype=np.int32)
+    asp = np.ascontiguousarray(anchor_suffix_ptr, dtype=np.int32)
+    so = np.ascontiguousarray(suffix_offsets, dtype=np.int32)
+    rank_of = np.zeros(max(ao.size - 1, 0), dtype=np.int32)
+    pairs = np.zeros(int(num_ranks), dtype=np.int64)
+    code = lib.quail_shard_anchors(int(ao.size - 1), ao.ctypes.data, asp.ctypes.data,
+                                   so.ctypes.data, int(num_ranks), rank_of.ctypes.data,
+                                   pairs.ctypes.data)
+    _check(code, "quail_shard_anchors")
+    return rank_of, pairs
+
+
+def shard_batch(anchor_offsets, anchor_suffix_ptr, suffix_offsets, rank_of_anchor, rank):
+    """One rank's sub-batch: its anchors in their original order with their suffixes.
+    Returns int32 offset arrays rebased to the sub-batch (anchor_offsets,
+    anchor_suffix_ptr, suffix_offsets, as quail_cascade_attn takes them) and int64 row
+    indices into the full batch: anchor_rows (rows of k_anc / v_anc) and suffix_rows
+    (rows of q_suf / k_suf / v_suf and of out / lse)."""
+    import numpy as np
+    ao = np.asarray(anchor_offsets, dtype=np.int64)
+    asp = np.asarray(anchor_suffix_ptr, dtype=np.int64)
+    so = np.asarray(suffix_offsets, dtype=np.int64)
+    mine = np.flatnonzero(np.asarray(rank_of_anchor) == rank)
+    la = ao[mine + 1] - ao[mine]
+    n_suf = asp[mine + 1] - asp[mine]
+    sufs = (np.concatenate([np.arange(asp[a], asp[a + 1]) for a in mine])
+            if mine.size else np.zeros(0, np.int64))
+    ls = so[sufs + 1] - so[sufs]
+    cat = lambda parts: np.concatenate(parts) if parts else np.zeros(0, np.int64)
+    anchor_rows = cat([np.arange(ao[a], ao[a + 1]) for a in mine])
+    suffix_rows = cat([np.arange(so[s], so[s + 1]) for s in sufs])
+    prefix = lambda x: np.concatenate([[0], np.cumsum(x)]).astype(np.int32)
+    return {"anchor_offsets": prefix(la), "anchor_suffix_ptr": prefix(n_suf),
+            "suffix_offsets": prefix(ls), "anchor_rows": anchor_rows.astype(np.int64),
+            "suffix_rows": suffix_rows.astype(np.int64), "anchors": mine.astype(np.int32)}
 
 
 def restricted_head(h, gamma, w8, logits, argmax, eps=1e-6, row_index=None, n_rows=None,
