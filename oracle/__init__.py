@@ -33,6 +33,9 @@ shard.py: sharding one batch over ranks by anchor (visible-pair work per anchor,
 longest-processing-time-first, the exhaustive optimum); pins in tests/test_oracle_shard.py
 (pair counts from the mask, Graham's bound against the optimum, a textbook worst case).
 
+join.py: the join's verdicts from the head's argmax (verdict per suffix, the passing
+suffixes in order, a count per anchor); pins in tests/test_oracle_join.py.
+
 Pins (tests/test_oracle.py): brute-force loops, the cascade-merge = monolithic identity,
 closed forms, a library SDPA with an explicit mask, RMSNorm closed forms, all 256 E4M3
 codes against the OCP formula and against torch's float8_e4m3fn. No function here is
