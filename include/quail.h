@@ -168,6 +168,32 @@ quail_status quail_kv_plan(int32_t num_anchors, const int64_t* anchor_tokens,
                            quail_kv_plan_stats* stats);
 
 /*
+ * Join verdicts from the head's argmax ([P1] "Como funciona": a boolean AI.IF needs only
+ * the one token of the last prefill pass, one of 8 options; [P2]'s AI_JOIN keeps the
+ * pairs for which it holds). Suffix s (one anchor-candidate pair) passes when
+ * argmax[s] == true_index. Device memory, asynchronous on `stream`.
+ *
+ *   anchor_suffix_ptr [A+1] int32: suffixes of anchor a are [ptr[a], ptr[a+1]); needed
+ *                     only with anchor_count
+ *   argmax    [S] int32, the restricted head's output for the last token of each suffix
+ *   true_index        the option (0..7) that stands for "true"
+ *   verdict   [S] uint8 out (1 = passes); may be NULL
+ *   selected  [S] int32 out: the passing suffix ids in increasing order (anchor-major);
+ *             entries past *num_selected are left as they were
+ *   num_selected [1] int32 out (device)
+ *   anchor_count [A] int32 out: passing suffixes per anchor; may be NULL
+ *   workspace  >= quail_join_select_workspace_size(S) bytes, 16-byte aligned
+ * Errors: QUAIL_ERR_INVALID_ARG for negative counts, true_index outside 0..7, NULL or
+ * misaligned (4-byte) arrays that the call needs, or a short workspace.
+ */
+size_t quail_join_select_workspace_size(int32_t num_suffixes);
+quail_status quail_join_select(int32_t num_anchors, int32_t num_suffixes,
+                               const int32_t* anchor_suffix_ptr, const int32_t* argmax,
+                               int32_t true_index, uint8_t* verdict, int32_t* selected,
+                               int32_t* num_selected, int32_t* anchor_count, void* workspace,
+                               size_t workspace_bytes, quail_stream_t stream);
+
+/*
  * Sharding one batch over ranks by anchor ([P1] "Como funciona", cascade-attention
  * bullet: a suffix attends only to its own anchor and to itself, so an anchor with its
  * suffixes is an independent unit and ranks exchange no data). HOST call on HOST memory

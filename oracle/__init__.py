@@ -45,6 +45,7 @@ from .attention import (anchor_partial, cascade_attention, cascade_suffix, lse_m
                         suffix_attention, suffix_partial)
 from .fp8 import dequantize_kv_fp8, e4m3_decode, e4m3_encode, quantize_kv_fp8
 from .head import restricted_head, rmsnorm, top2_margin
+from .join import join_select
 
 __all__ = [
     "anchor_partial", "cascade_attention", "cascade_suffix", "lse_merge", "suffix_attention",

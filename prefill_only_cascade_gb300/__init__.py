@@ -33,6 +33,7 @@ EXPORTED_SYMBOLS = (
     "quail_set_wait_timeout_ns", "quail_debug_inject", "quail_version",
     "quail_cascade_attn_noalloc", "quail_causal_prefill_attn",
     "quail_causal_prefill_workspace_size", "quail_kv_plan", "quail_shard_anchors",
+    "quail_join_select", "quail_join_select_workspace_size",
 )
 
 
@@ -108,6 +109,11 @@ def _load():
     lib.quail_kv_plan.restype = ctypes.c_int
     lib.quail_shard_anchors.argtypes = [i32, vp, vp, vp, i32, vp, vp]
     lib.quail_shard_anchors.restype = ctypes.c_int
+    lib.quail_join_select_workspace_size.argtypes = [i32]
+    lib.quail_join_select_workspace_size.restype = ctypes.c_size_t
+    lib.quail_join_select.argtypes = [i32, i32, vp, vp, i32, vp, vp, vp, vp, vp,
+                                      ctypes.c_size_t, vp]
+    lib.quail_join_select.restype = ctypes.c_int
     return lib
 
 
@@ -263,6 +269,23 @@ def restricted_head(h, gamma, w8, logits, argmax, eps=1e-6, row_index=None, n_ro
                                    int(h.stride(0)), _ptr(row_index), _ptr(gamma), _ptr(w8),
                                    _ptr(logits), _ptr(argmax), _stream(stream))
     _check(st, "quail_restricted_head")
+
+
+def join_select_workspace_size(num_suffixes) -> int:
+    return int(lib.quail_join_select_workspace_size(int(num_suffixes)))
+
+
+def join_select(argmax, true_index, selected, num_selected, workspace, verdict=None,
+                anchor_suffix_ptr=None, anchor_count=None, stream=None):
+    """quail_join_select on torch CUDA tensors: verdicts of the head's argmax, the passing
+    suffix ids in increasing order, their number, and (optionally) a count per anchor."""
+    num_anchors = 0 if anchor_suffix_ptr is None else int(anchor_suffix_ptr.numel() - 1)
+    st = lib.quail_join_select(num_anchors, int(argmax.numel()), _ptr(anchor_suffix_ptr),
+                               _ptr(argmax), int(true_index), _ptr(verdict), _ptr(selected),
+                               _ptr(num_selected), _ptr(anchor_count), _ptr(workspace),
+                               int(workspace.numel() * workspace.element_size()),
+                               _stream(stream))
+    _check(st, "quail_join_select")
 
 
 def quantize_kv_fp8(kv_bf16, anchor_offsets, codes, scale, stream=None):

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libquail.so")
 SOURCES = ["api.cu", "cascade.cu", "head.cu", "kv_plan.cu", "noalloc.cu", "prefill.cu",
-           "quantize.cu", "shard.cu"]
+           "quantize.cu", "select.cu", "shard.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -290,6 +290,41 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
   return e == cudaSuccess ? QUAIL_OK : QUAIL_ERR_CUDA;
 }
 
+size_t quail_join_select_workspace_size(int32_t num_suffixes) {
+  return num_suffixes < 0 ? 0 : quail::join_select_workspace_bytes(num_suffixes);
+}
+
+quail_status quail_join_select(int32_t num_anchors, int32_t num_suffixes,
+                               const int32_t* anchor_suffix_ptr, const int32_t* argmax,
+                               int32_t true_index, uint8_t* verdict, int32_t* selected,
+                               int32_t* num_selected, int32_t* anchor_count, void* workspace,
+                               size_t workspace_bytes, quail_stream_t stream) {
+  if (num_anchors < 0 || num_suffixes < 0 || true_index < 0 || true_index > 7)
+    return QUAIL_ERR_INVALID_ARG;
+  if (num_selected == nullptr || (reinterpret_cast<uintptr_t>(num_selected) & 3u))
+    return QUAIL_ERR_INVALID_ARG;
+  if (num_suffixes > 0 &&
+      (argmax == nullptr || selected == nullptr ||
+       ((reinterpret_cast<uintptr_t>(argmax) | reinterpret_cast<uintptr_t>(selected)) & 3u)))
+    return QUAIL_ERR_INVALID_ARG;
+  if (anchor_count != nullptr && num_anchors > 0 &&
+      (anchor_suffix_ptr == nullptr ||
+       ((reinterpret_cast<uintptr_t>(anchor_count) |
+         reinterpret_cast<uintptr_t>(anchor_suffix_ptr)) & 3u)))
+    return QUAIL_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < quail::join_select_workspace_bytes(num_suffixes) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 15u))
+    return QUAIL_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  const quail_status ds = device_state(&st);
+  if (ds != QUAIL_OK) return ds;
+  quail::JoinSelectArgs j{num_anchors, num_suffixes, anchor_suffix_ptr, argmax, true_index,
+                          verdict, selected, num_selected, anchor_count,
+                          static_cast<int32_t*>(workspace)};
+  const cudaError_t e = quail::launch_join_select(j, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QUAIL_OK : QUAIL_ERR_CUDA;
+}
+
 quail_status quail_restricted_head(int64_t n_rows, int32_t hidden, float eps, const void* h,
                                    int64_t h_row_stride, const int32_t* row_index,
                                    const void* gamma, const void* w8, float* logits,

@@ -34,6 +34,21 @@ struct QuantArgs {
 };
 cudaError_t launch_quantize_kv_fp8(const QuantArgs& q, int num_sms, cudaStream_t stream);
 
+struct JoinSelectArgs {
+  int num_anchors;
+  int64_t num_suffixes;
+  const int32_t* anchor_suffix_ptr;
+  const int32_t* argmax;
+  int32_t true_index;
+  uint8_t* verdict;
+  int32_t* selected;
+  int32_t* num_selected;
+  int32_t* anchor_count;
+  int32_t* chunk_work;  // workspace: one int32 per chunk of suffixes
+};
+size_t join_select_workspace_bytes(int64_t num_suffixes);
+cudaError_t launch_join_select(const JoinSelectArgs& j, cudaStream_t stream);
+
 // Everything the cascade kernels need besides the tensor maps.
 struct CascadeParams {
   int num_anchors, num_suffixes;

@@ -157,3 +157,21 @@ def test_causal_prefill_rejects_bad_arguments():
     assert call(ws_bytes=64) == q.QUAIL_ERR_INVALID_ARG     # workspace too small
     assert q.causal_prefill_workspace_size(3, 100, 60, 8, 2, 128) > 256
     assert q.causal_prefill_workspace_size(-1, 100, 60, 8, 2, 128) == 0
+
+
+def test_join_select_rejects_bad_arguments():
+    f = ctypes.c_void_p(0x10000)
+    ws_need = q.join_select_workspace_size(10)
+    assert ws_need >= 16 and q.join_select_workspace_size(-1) == 0
+    call = lambda **kw: q.lib.quail_join_select(
+        kw.get("A", 2), kw.get("S", 10), kw.get("asp", f), kw.get("am", f), kw.get("t", 3),
+        kw.get("v", None), kw.get("sel", f), kw.get("n", f), kw.get("cnt", None),
+        kw.get("ws", f), ctypes.c_size_t(kw.get("ws_bytes", ws_need)), None)
+    assert call(t=8) == q.QUAIL_ERR_INVALID_ARG            # only 8 options
+    assert call(t=-1) == q.QUAIL_ERR_INVALID_ARG
+    assert call(S=-1) == q.QUAIL_ERR_INVALID_ARG
+    assert call(n=None) == q.QUAIL_ERR_INVALID_ARG         # the count is always written
+    assert call(am=None) == q.QUAIL_ERR_INVALID_ARG
+    assert call(sel=ctypes.c_void_p(0x10002)) == q.QUAIL_ERR_INVALID_ARG   # misaligned
+    assert call(cnt=f, asp=None) == q.QUAIL_ERR_INVALID_ARG  # per-anchor counts need the CSR
+    assert call(ws_bytes=ws_need - 4) == q.QUAIL_ERR_INVALID_ARG
