@@ -89,3 +89,21 @@ def test_model_time_grows_with_work_and_beats_nothing_below_sol():
     for r in (small, big):
         assert r["model_seconds"] >= r["mma_floor_seconds"] >= 0.9 * r["sol_seconds"]
         assert r["bound"] == "tensor"
+
+
+def test_visible_pairs_agree_across_bench_cost_model_and_oracle():
+    # three independent countings of the visible (query, key) pairs: the bench's FLOP
+    # count, the cost model's work, and the sharding oracle's per-anchor work
+    import bench
+    from oracle import shard
+    rng = np.random.default_rng(31)
+    for _ in range(10):
+        A = int(rng.integers(1, 9))
+        counts = rng.integers(0, 7, size=A)
+        lay = workloads.layout_from_lengths(rng.integers(0, 500, size=A), counts,
+                                            rng.integers(1, 70, size=int(counts.sum())))
+        pairs = sum(shard.anchor_pairs(lay.anchor_offsets, lay.anchor_suffix_ptr,
+                                       lay.suffix_offsets))
+        w = cm.work(lay.anchor_offsets, lay.anchor_suffix_ptr, lay.suffix_offsets, 32, 8, 128)
+        assert w["visible_pairs"] == pairs
+        assert bench.attention_flops(lay, 32, 128) == 4 * 128 * 32 * pairs
