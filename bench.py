@@ -195,11 +195,12 @@ def rank_workload(cfg, rank: int):
 # ---------------------------------------------------------------------------- oracle timing
 
 def cpu_oracle_sample(layout, cfg, t_host_fn, budget_s=15.0, max_suffixes=1024, kv_for=None,
-                      with_head=True):
+                      with_head=True, results=None):
     """Time the float64 oracle (attention of each suffix + its head row) on host cores over a
     seeded sample of suffixes until `budget_s` is spent. kv_for(anchor) -> (k, v) float64
     replaces the anchor K/V (FP8: the oracle quantises and dequantises the anchor itself,
-    once per anchor, inside the timed loop). Returns tokens/s and details."""
+    once per anchor, inside the timed loop). With a dict `results`, each sampled suffix's
+    oracle (out, lse) is stored under its id. Returns tokens/s and details."""
     import oracle
     try:
         from threadpoolctl import threadpool_info
@@ -223,7 +224,9 @@ def cpu_oracle_sample(layout, cfg, t_host_fn, budget_s=15.0, max_suffixes=1024, 
             if c["anchor"] not in kv_cache:
                 kv_cache[c["anchor"]] = kv_for(c["anchor"])
             ka, va = kv_cache[c["anchor"]]
-        oracle.suffix_attention(c["q_suf"], ka, va, c["k_suf"], c["v_suf"], scale)
+        ref = oracle.suffix_attention(c["q_suf"], ka, va, c["k_suf"], c["v_suf"], scale)
+        if results is not None:
+            results[int(s)] = (c["rows"], ref)
         if with_head:
             oracle.restricted_head(h64[j:j + 1], g64, w64, 1e-6)
         tokens += c["rows"][1] - c["rows"][0]
@@ -249,6 +252,32 @@ def fp8_oracle_kv(t_bf16, layout):
             pair.append(oracle.dequantize_kv_fp8(codes, scales, np.array([0, hi - lo])))
         return tuple(pair)
     return kv_for
+
+
+def sampled_parity(results, out, lse):
+    """Errors of the timed call's output against the oracle on the sampled suffixes."""
+    if not results:
+        return None
+    try:
+        return _sampled_parity(results, out, lse)
+    except Exception as e:  # a reporting aid: never fail the measurement over it
+        print(f"parity figures unavailable: {e}", file=sys.stderr)
+        return None
+
+
+def _sampled_parity(results, out, lse):
+    g_o, r_o, g_l, r_l = [], [], [], []
+    for (r0, r1), (ro, rl) in results.values():
+        if r1 == r0:
+            continue
+        g_o.append(out[r0:r1].to("cpu", torch.float64).numpy())
+        g_l.append(lse[r0:r1].to("cpu", torch.float64).numpy())
+        r_o.append(ro)
+        r_l.append(rl)
+    go, ro_, gl, rl_ = (np.concatenate(x) for x in (g_o, r_o, g_l, r_l))
+    return {"suffixes": len(results), "max_abs": float(np.abs(go - ro_).max()),
+            "rel_l2": float(np.linalg.norm(go - ro_) / max(np.linalg.norm(ro_), 1e-30)),
+            "lse_abs": float(np.abs(gl - rl_).max())}
 
 
 def run_reference(args):
@@ -420,11 +449,15 @@ def run_ours(args):
         e2e = run_e2e(args, q, desc, layout, t, hx, last, k_scale, v_scale, dev, stream, world)
 
     cpu = None
+    parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         def host_cases(ids):
             return workloads.gather_suffix_case(t_bf16, layout, ids)
+        parity_refs = {}
         v, cores, sample, dt = cpu_oracle_sample(
-            layout, cfg, host_cases, kv_for=fp8_oracle_kv(t_bf16, layout) if kv_fp8 else None)
+            layout, cfg, host_cases, kv_for=fp8_oracle_kv(t_bf16, layout) if kv_fp8 else None,
+            results=parity_refs)
+        parity = sampled_parity(parity_refs, out, lse)
         cpu = {"value": v, "unit": "suffix tokens/s", "cores": cores, "kind": "oracle",
                "sample": sample + (" (the oracle quantises each sampled anchor itself)"
                                    if kv_fp8 else ""), "seconds": round(dt, 2)}
@@ -442,6 +475,8 @@ def run_ours(args):
                    "head_hidden": hcfg.hidden, "head_rows": S,
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cost_model": model, "cpu_baseline": cpu, "e2e": e2e,
+        # the timed call's output against the oracle on the CPU baseline's sampled suffixes
+        "parity": parity,
         # per step: segments, schedule, items, (FP8: anchor staging), fast + exact cascade
         # kernels, head
         "gpu_launches": (7 if kv_fp8 and layout.total_anchor_tokens > 0 else 6) * args.steps,
@@ -636,9 +671,11 @@ def run_prefill(args):
     if not args.no_cpu_baseline:
         # the oracle on one seeded sequence at least (each is 4,096 tokens of causal
         # attention: ~20 s of float64 work on the host cores)
+        parity_refs = {}
         v, cores, sample, dt = cpu_oracle_sample(
             lay, cfg, lambda ids: workloads.gather_suffix_case(t, lay, ids), budget_s=15.0,
-            max_suffixes=4, with_head=False)
+            max_suffixes=4, with_head=False, results=parity_refs)
+        line["parity"] = sampled_parity(parity_refs, out, lse)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": sample, "seconds": round(dt, 2)}
     from prefill_only_cascade_gb300 import cost_model
