@@ -63,3 +63,33 @@ def test_noalloc_rejects_batches_beyond_the_scratch_array():
     with pytest.raises(q.QuailError) as e:
         q.cascade_attn_noalloc(desc, *([None] * 8), out=None)
     assert e.value.status == q.QUAIL_ERR_UNSUPPORTED
+
+
+def test_noalloc_fp8_stages_the_anchors_in_the_scratch_array():
+    # FP8 anchor KV: the bf16 staging of the anchor codes also lives in the fixed array
+    import numpy as np
+    import prefill_only_cascade_gb300 as q
+    heads = (32, 8, 128)
+    rng = np.random.default_rng(78)
+    lay, t = _case([300, 129, 0], [6, 4, 2], rng.integers(1, 40, size=12), heads, 23)
+    codes, scales = {}, {}
+    for name in ("k_anc", "v_anc"):
+        c = torch.empty(t[name].shape, dtype=torch.uint8, device="cuda")
+        sc = torch.empty(lay.num_anchors, 8, dtype=torch.float32, device="cuda")
+        q.quantize_kv_fp8(t[name], t["anchor_offsets"], c, sc)
+        codes[name], scales[name] = c, sc
+    t8 = dict(t, k_anc=codes["k_anc"], v_anc=codes["v_anc"])
+    ref_out, ref_lse = run_cascade(heads, lay, t8, kv_fp8=True, k_scale=scales["k_anc"],
+                                   v_scale=scales["v_anc"])
+    desc = q.make_desc(lay.num_anchors, lay.num_suffixes, lay.total_anchor_tokens,
+                       lay.total_suffix_tokens, lay.max_anchor_len, lay.max_suffix_len,
+                       *heads, 0.0, True)
+    assert q.cascade_workspace_size(desc) <= 64 * 1024 * 1024
+    out = torch.full_like(ref_out, float("nan"))
+    lse = torch.full_like(ref_lse, float("nan"))
+    q.cascade_attn_noalloc(desc, t8["q_suf"], t8["k_anc"], t8["v_anc"], t8["k_suf"],
+                           t8["v_suf"], t8["anchor_offsets"], t8["anchor_suffix_ptr"],
+                           t8["suffix_offsets"], out, lse, scales["k_anc"], scales["v_anc"])
+    torch.cuda.synchronize()
+    assert q.get_device_error() == q.QUAIL_OK
+    compare(np64(out), np64(lse), np64(ref_out), np64(ref_lse))
