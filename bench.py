@@ -559,6 +559,48 @@ def run_e2e(args, q, desc, layout, t, hx, last, k_scale, v_scale, dev, stream, w
             "overlap": "inputs of step i + 1 copied on a second stream during step i"}
 
 
+def head_oracle_sample(h, gamma, w8, eps, logits, argmax, rows=65536):
+    """The oracle's RMSNorm + 8-column head on the first `rows` rows (host cores, timed),
+    and the kernel's output there against it: logits max |err|, argmax agreement where
+    the oracle's top-2 margin exceeds 1e-2."""
+    import oracle
+    n = min(rows, h.shape[0])
+    h64 = h[:n].to("cpu", torch.float64).numpy()
+    g64, w64 = gamma.to("cpu", torch.float64).numpy(), w8.to("cpu", torch.float64).numpy()
+    t0 = time.perf_counter()
+    ref_logits, ref_am = oracle.restricted_head(h64, g64, w64, eps)
+    dt = time.perf_counter() - t0
+    lg = logits[:n].to("cpu", torch.float64).numpy()
+    am = argmax[:n].cpu().numpy()
+    sure = oracle.top2_margin(ref_logits) > 1e-2
+    cpu = {"value": n / dt, "unit": "rows/s", "cores": len(os.sched_getaffinity(0)),
+           "kind": "oracle", "sample": f"the first {n} rows", "seconds": round(dt, 2)}
+    parity = {"rows": n, "logits_max_abs": float(np.abs(lg - ref_logits).max()),
+              "argmax_checked": int(sure.sum()),
+              "argmax_mismatches": int((am[sure] != ref_am[sure]).sum())}
+    return cpu, parity
+
+
+def quantize_oracle_sample(kv, anchor_offsets, codes, scale, anchors=8):
+    """The oracle's E4M3 quantisation of the first `anchors` anchors (host cores, timed),
+    and the kernel's codes and scales there against it, bit for bit."""
+    import oracle
+    hi = int(anchor_offsets[anchors])
+    x = kv[:hi].to("cpu", torch.float32).numpy()
+    t0 = time.perf_counter()
+    ref_codes, ref_scale = oracle.quantize_kv_fp8(x, np.asarray(anchor_offsets[:anchors + 1]))
+    dt = time.perf_counter() - t0
+    got_codes = codes[:hi].cpu().numpy()
+    got_scale = scale[:anchors].cpu().numpy()
+    cpu = {"value": x.size / dt, "unit": "elements/s", "cores": len(os.sched_getaffinity(0)),
+           "kind": "oracle", "sample": f"the first {anchors} anchor(s), {x.size} elements",
+           "seconds": round(dt, 2)}
+    parity = {"elements": int(x.size),
+              "code_mismatches": int((got_codes != ref_codes).sum()),
+              "scale_mismatches": int((got_scale != ref_scale).sum())}
+    return cpu, parity
+
+
 def run_bandwidth_kernel(args):
     """Per-kernel measurement of the HBM-bound kernels (not the headline step):
     --workload head      restricted head on 2,000,000 rows x 2,560 (bf16)
@@ -607,6 +649,12 @@ def run_bandwidth_kernel(args):
         torch.cuda.synchronize()
     ms = statistics.median(a.elapsed_time(b) for a, b in evs)
     gbs = algo_bytes / (ms / 1e3) / 1e9
+    cpu = parity = None
+    if not args.no_cpu_baseline:
+        if args.workload == "head":
+            cpu, parity = head_oracle_sample(x["h"], x["gamma"], x["w8"], cfg.eps, logits, am)
+        else:
+            cpu, parity = quantize_oracle_sample(kv, lay.anchor_offsets, codes, scale)
     line = {"metric": f"{args.workload} kernel throughput", "value": units / (ms / 1e3),
             "unit": unit, "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
             "ms_per_step": ms, "higher_is_better": True, "data": "synthetic",
@@ -615,7 +663,7 @@ def run_bandwidth_kernel(args):
                          "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
                          "peak_source": f"hbm_gbs of {src}", "kernel": kernel,
                          "algorithmic_bytes_per_launch": algo_bytes},
-            "clocks": clk.summary()}
+            "cpu_baseline": cpu, "parity": parity, "clocks": clk.summary()}
     print(json.dumps(line))
 
 
