@@ -13,6 +13,7 @@ float64 CPU oracle on a bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -280,12 +281,26 @@ def _sampled_parity(results, out, lse):
             "lse_abs": float(np.abs(gl - rl_).max())}
 
 
+def attention_config(cfg, layout, world):
+    """The `config` object of an attention workload's line (both arms)."""
+    hcfg = workloads.HEAD_CONFIGS["join_last_token"]
+    return {"workload": cfg.name, "anchors": cfg.num_anchors,
+            "anchor_len": list(cfg.anchor_len), "suffixes_per_anchor": cfg.suffixes_per_anchor,
+            "suffix_len": list(cfg.suffix_len), "q_heads": cfg.num_q_heads,
+            "kv_heads": cfg.num_kv_heads, "head_dim": cfg.head_dim,
+            "suffix_tokens": layout.total_suffix_tokens, "head_hidden": hcfg.hidden,
+            "head_rows": layout.num_suffixes, "l2": "inputs larger than L2 (no flush)",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args):
     """--impl reference: the float64 CPU oracle, as it stands, on the host cores."""
     world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
     if rank != 0:
         return
     cfg = workloads.ATTN_CONFIGS[args.workload]
+    if args.suffixes_per_anchor:
+        cfg = dataclasses.replace(cfg, suffixes_per_anchor=args.suffixes_per_anchor)
     layout = workloads.make_layout(cfg)
     # a bounded per-step sample: the same seeded suffixes every step, generated on the host
     ids = workloads.sample_suffixes(layout, 48, cfg.seed + 200)
@@ -321,8 +336,8 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{cfg.name} (bounded sample)", "sample_suffixes": int(sub.num_suffixes),
-                   "sample_tokens": int(sub.total_suffix_tokens)},
+        # our arm's workload; every step times a bounded sample of it (cpu_baseline.sample)
+        "config": attention_config(cfg, layout, world),
         "cpu_baseline": {"value": value, "unit": "suffix tokens/s", "cores": cores,
                          "kind": "oracle",
                          "sample": f"{sub.num_suffixes} seeded suffixes ({sub.total_suffix_tokens} tokens) "
@@ -468,12 +483,7 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 (fp32 accumulate)" if not kv_fp8 else "bf16 Q / e4m3 anchor KV",
         "data": "synthetic (seeded N(0,1) bf16)",
-        "config": {"workload": cfg.name, "anchors": cfg.num_anchors,
-                   "anchor_len": list(cfg.anchor_len), "suffixes_per_anchor": cfg.suffixes_per_anchor,
-                   "suffix_len": list(cfg.suffix_len), "q_heads": hq, "kv_heads": hkv,
-                   "head_dim": d, "suffix_tokens": layout.total_suffix_tokens,
-                   "head_hidden": hcfg.hidden, "head_rows": S,
-                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "config": attention_config(cfg, layout, world),
         "roofline": roofline, "cost_model": model, "cpu_baseline": cpu, "e2e": e2e,
         # the timed call's output against the oracle on the CPU baseline's sampled suffixes
         "parity": parity,
