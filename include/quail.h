@@ -217,6 +217,39 @@ quail_status quail_shard_anchors(int32_t num_anchors, const int32_t* anchor_offs
                                  const int32_t* suffix_offsets, int32_t num_ranks,
                                  int32_t* rank_of_anchor, int64_t* rank_pairs);
 
+/*
+ * One rank's sub-batch of a batch split by quail_shard_anchors. HOST call on HOST memory
+ * (no GPU work). The rank's anchors, in their original order, each with all of its
+ * suffixes, as a batch that quail_cascade_attn takes, plus the rows of the full batch's
+ * tensors that the sub-batch reads and writes.
+ *
+ *   anchor_offsets [A+1], anchor_suffix_ptr [A+1] (anchor_suffix_ptr[0] == 0),
+ *   suffix_offsets [S+1]: int32, as for quail_cascade_attn (lengths >= 0)
+ *   rank_of_anchor [A] int32, e.g. from quail_shard_anchors; rank >= 0
+ *   sizes     out (always written): the sub-batch's anchors, suffixes, anchor tokens and
+ *             suffix tokens
+ *   The six arrays below are either all NULL (size query) or all given, sized from
+ *   `sizes`:
+ *   sub_anchor_offsets [A_r+1], sub_anchor_suffix_ptr [A_r+1], sub_suffix_offsets [S_r+1]
+ *             int32 out: the sub-batch's offsets (prefix sums from 0)
+ *   anchors     [A_r] int32 out: full-batch index of each kept anchor
+ *   anchor_rows [T_A,r] int64 out: rows of k_anc / v_anc, in sub-batch order
+ *   suffix_rows [T_S,r] int64 out: rows of q_suf / k_suf / v_suf (and of out / lse)
+ * Errors: QUAIL_ERR_INVALID_ARG for negative counts or lengths, NULL inputs or sizes, some
+ * but not all output arrays, or anchor_suffix_ptr[0] != 0; QUAIL_ERR_UNSUPPORTED when a
+ * sub-batch token count exceeds int32 offsets.
+ */
+typedef struct {
+  int32_t num_anchors, num_suffixes;
+  int64_t anchor_tokens, suffix_tokens;
+} quail_shard_sizes;
+quail_status quail_shard_batch(int32_t num_anchors, const int32_t* anchor_offsets,
+                               const int32_t* anchor_suffix_ptr, const int32_t* suffix_offsets,
+                               const int32_t* rank_of_anchor, int32_t rank,
+                               quail_shard_sizes* sizes, int32_t* sub_anchor_offsets,
+                               int32_t* sub_anchor_suffix_ptr, int32_t* sub_suffix_offsets,
+                               int32_t* anchors, int64_t* anchor_rows, int64_t* suffix_rows);
+
 /* Size of the library's fixed device scratch array used by quail_cascade_attn_noalloc. */
 #define QUAIL_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 
@@ -254,15 +287,19 @@ quail_status quail_cascade_attn_noalloc(const quail_cascade_desc* desc, const vo
  *
  *   h        bf16 rows of `hidden` elements, row r at h + r * h_row_stride elements;
  *            h_row_stride >= hidden, (h_row_stride * 2) % 16 == 0
- *   row_index int32 [n_rows] source rows (e.g. the last token of each suffix), or NULL
+ *   h_rows   number of rows of h (>= 0); without row_index, n_rows <= h_rows
+ *   row_index int32 [n_rows] source rows (e.g. the last token of each suffix), or NULL.
+ *            Checked on the device: an index outside [0, h_rows) reads nothing, its row
+ *            gets NaN logits and argmax -1, and quail_get_device_error() then reports
+ *            QUAIL_ERR_DEVICE_BOUNDS.
  *   gamma    bf16 [hidden]; w8 bf16 [8, hidden] row-major
  *   logits   fp32 [n_rows, 8]; argmax int32 [n_rows]
  * hidden must be a positive multiple of 32 and at most 6144. n_rows may be 0.
  */
 quail_status quail_restricted_head(int64_t n_rows, int32_t hidden, float eps, const void* h,
-                                   int64_t h_row_stride, const int32_t* row_index,
-                                   const void* gamma, const void* w8, float* logits,
-                                   int32_t* argmax, quail_stream_t stream);
+                                   int64_t h_rows, int64_t h_row_stride,
+                                   const int32_t* row_index, const void* gamma, const void* w8,
+                                   float* logits, int32_t* argmax, quail_stream_t stream);
 
 /*
  * Per-(anchor, KV head) E4M3 quantisation of anchor K or V (the FP8 KV of the
@@ -271,7 +308,7 @@ quail_status quail_restricted_head(int64_t n_rows, int32_t hidden, float eps, co
  *   and all d; code = e4m3(x / scale), x / scale rounded to fp32 first, then rounded to
  *   nearest even with saturation at +-448 (sign kept).
  *   kv_bf16 [T_A, Hkv, d] bf16 in; kv_e4m3 [T_A, Hkv, d] codes out; scale [A, Hkv] fp32
- *   out. d in {64, 128}, Hkv * d <= 4096. A memset and three small kernels on `stream`.
+ *   out. d in {64, 128}, Hkv * d <= 4096. One kernel (clusters of CTAs) on `stream`.
  */
 quail_status quail_quantize_kv_fp8(int32_t num_anchors, const int32_t* anchor_offsets,
                                    int64_t total_anchor_tokens, int32_t num_kv_heads,

@@ -59,3 +59,26 @@ def optimal_makespan(costs, num_ranks):
         m = max(loads)
         best = m if best is None else min(best, m)
     return best if best is not None else 0
+
+
+def sub_batch(anchor_offsets, anchor_suffix_ptr, suffix_offsets, rank_of_anchor, rank):
+    """One rank's sub-batch, written out plainly: the anchors assigned to `rank` in their
+    original order, each with all of its suffixes; offsets are the prefix sums of the kept
+    lengths, and rows list, in that order, the full batch's anchor rows and suffix rows
+    that the sub-batch covers."""
+    ao = [int(x) for x in anchor_offsets]
+    asp = [int(x) for x in anchor_suffix_ptr]
+    so = [int(x) for x in suffix_offsets]
+    res = {"anchor_offsets": [0], "anchor_suffix_ptr": [0], "suffix_offsets": [0],
+           "anchors": [], "anchor_rows": [], "suffix_rows": []}
+    for a in range(len(ao) - 1):
+        if int(rank_of_anchor[a]) != rank:
+            continue
+        res["anchors"].append(a)
+        res["anchor_rows"].extend(range(ao[a], ao[a + 1]))
+        res["anchor_offsets"].append(len(res["anchor_rows"]))
+        for s in range(asp[a], asp[a + 1]):
+            res["suffix_rows"].extend(range(so[s], so[s + 1]))
+            res["suffix_offsets"].append(len(res["suffix_rows"]))
+        res["anchor_suffix_ptr"].append(len(res["suffix_offsets"]) - 1)
+    return res

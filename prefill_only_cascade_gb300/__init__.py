@@ -33,7 +33,7 @@ EXPORTED_SYMBOLS = (
     "quail_set_wait_timeout_ns", "quail_debug_inject", "quail_version",
     "quail_cascade_attn_noalloc", "quail_causal_prefill_attn",
     "quail_causal_prefill_workspace_size", "quail_kv_plan", "quail_shard_anchors",
-    "quail_join_select", "quail_join_select_workspace_size",
+    "quail_join_select", "quail_join_select_workspace_size", "quail_shard_batch",
 )
 
 
@@ -41,6 +41,11 @@ class QuailError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
         super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class ShardSizes(ctypes.Structure):
+    _fields_ = [("num_anchors", ctypes.c_int32), ("num_suffixes", ctypes.c_int32),
+                ("anchor_tokens", ctypes.c_int64), ("suffix_tokens", ctypes.c_int64)]
 
 
 class KvPlanStats(ctypes.Structure):
@@ -84,7 +89,8 @@ def _load():
     lib.quail_cascade_workspace_size.argtypes = [ctypes.POINTER(CascadeDesc)]
     lib.quail_cascade_workspace_size.restype = ctypes.c_size_t
     lib.quail_restricted_head.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_float, vp,
-                                          ctypes.c_int64, i32p, vp, vp, f32p, i32p, vp]
+                                          ctypes.c_int64, ctypes.c_int64, i32p, vp, vp, f32p,
+                                          i32p, vp]
     lib.quail_restricted_head.restype = ctypes.c_int
     lib.quail_quantize_kv_fp8.argtypes = [ctypes.c_int32, i32p, ctypes.c_int64, ctypes.c_int32,
                                           ctypes.c_int32, vp, vp, f32p, vp]
@@ -109,6 +115,9 @@ def _load():
     lib.quail_kv_plan.restype = ctypes.c_int
     lib.quail_shard_anchors.argtypes = [i32, vp, vp, vp, i32, vp, vp]
     lib.quail_shard_anchors.restype = ctypes.c_int
+    lib.quail_shard_batch.argtypes = [i32, vp, vp, vp, vp, i32, ctypes.POINTER(ShardSizes),
+                                      vp, vp, vp, vp, vp, vp]
+    lib.quail_shard_batch.restype = ctypes.c_int
     lib.quail_join_select_workspace_size.argtypes = [i32]
     lib.quail_join_select_workspace_size.restype = ctypes.c_size_t
     lib.quail_join_select.argtypes = [i32, i32, vp, vp, i32, vp, vp, vp, vp, vp,
@@ -235,39 +244,43 @@ def shard_anchors(anchor_offsets, anchor_suffix_ptr, suffix_offsets, num_ranks):
 
 
 def shard_batch(anchor_offsets, anchor_suffix_ptr, suffix_offsets, rank_of_anchor, rank):
-    """One rank's sub-batch: its anchors in their original order with their suffixes.
-    Returns int32 offset arrays rebased to the sub-batch (anchor_offsets,
-    anchor_suffix_ptr, suffix_offsets, as quail_cascade_attn takes them) and int64 row
-    indices into the full batch: anchor_rows (rows of k_anc / v_anc) and suffix_rows
-    (rows of q_suf / k_suf / v_suf and of out / lse)."""
+    """quail_shard_batch on host arrays: one rank's sub-batch (its anchors in their original
+    order with their suffixes). Returns int32 offset arrays rebased to the sub-batch
+    (anchor_offsets, anchor_suffix_ptr, suffix_offsets, as quail_cascade_attn takes them),
+    the kept anchors' ids and int64 row indices into the full batch: anchor_rows (rows of
+    k_anc / v_anc) and suffix_rows (rows of q_suf / k_suf / v_suf and of out / lse)."""
     import numpy as np
-    ao = np.asarray(anchor_offsets, dtype=np.int64)
-    asp = np.asarray(anchor_suffix_ptr, dtype=np.int64)
-    so = np.asarray(suffix_offsets, dtype=np.int64)
-    mine = np.flatnonzero(np.asarray(rank_of_anchor) == rank)
-    la = ao[mine + 1] - ao[mine]
-    n_suf = asp[mine + 1] - asp[mine]
-    sufs = (np.concatenate([np.arange(asp[a], asp[a + 1]) for a in mine])
-            if mine.size else np.zeros(0, np.int64))
-    ls = so[sufs + 1] - so[sufs]
-    cat = lambda parts: np.concatenate(parts) if parts else np.zeros(0, np.int64)
-    anchor_rows = cat([np.arange(ao[a], ao[a + 1]) for a in mine])
-    suffix_rows = cat([np.arange(so[s], so[s + 1]) for s in sufs])
-    prefix = lambda x: np.concatenate([[0], np.cumsum(x)]).astype(np.int32)
-    return {"anchor_offsets": prefix(la), "anchor_suffix_ptr": prefix(n_suf),
-            "suffix_offsets": prefix(ls), "anchor_rows": anchor_rows.astype(np.int64),
-            "suffix_rows": suffix_rows.astype(np.int64), "anchors": mine.astype(np.int32)}
+    ao = np.ascontiguousarray(anchor_offsets, dtype=np.int32)
+    asp = np.ascontiguousarray(anchor_suffix_ptr, dtype=np.int32)
+    so = np.ascontiguousarray(suffix_offsets, dtype=np.int32)
+    ro = np.ascontiguousarray(rank_of_anchor, dtype=np.int32)
+    A = int(ao.size - 1)
+    sz = ShardSizes()
+    args = (A, ao.ctypes.data, asp.ctypes.data, so.ctypes.data, ro.ctypes.data, int(rank))
+    _check(lib.quail_shard_batch(*args, ctypes.byref(sz), None, None, None, None, None, None),
+           "quail_shard_batch")
+    out = {"anchor_offsets": np.zeros(sz.num_anchors + 1, np.int32),
+           "anchor_suffix_ptr": np.zeros(sz.num_anchors + 1, np.int32),
+           "suffix_offsets": np.zeros(sz.num_suffixes + 1, np.int32),
+           "anchors": np.zeros(sz.num_anchors, np.int32),
+           "anchor_rows": np.zeros(sz.anchor_tokens, np.int64),
+           "suffix_rows": np.zeros(sz.suffix_tokens, np.int64)}
+    _check(lib.quail_shard_batch(*args, ctypes.byref(sz), *(out[k].ctypes.data for k in (
+        "anchor_offsets", "anchor_suffix_ptr", "suffix_offsets", "anchors", "anchor_rows",
+        "suffix_rows"))), "quail_shard_batch")
+    return out
 
 
 def restricted_head(h, gamma, w8, logits, argmax, eps=1e-6, row_index=None, n_rows=None,
                     stream=None):
     """quail_restricted_head: RMSNorm + 8-column head + argmax over rows of h (or over
-    h[row_index])."""
+    h[row_index]; indices outside h's rows are reported on the device, not read)."""
     if n_rows is None:
         n_rows = row_index.numel() if row_index is not None else h.shape[0]
     st = lib.quail_restricted_head(int(n_rows), int(h.shape[-1]), float(eps), _ptr(h),
-                                   int(h.stride(0)), _ptr(row_index), _ptr(gamma), _ptr(w8),
-                                   _ptr(logits), _ptr(argmax), _stream(stream))
+                                   int(h.shape[0]), int(h.stride(0)), _ptr(row_index),
+                                   _ptr(gamma), _ptr(w8), _ptr(logits), _ptr(argmax),
+                                   _stream(stream))
     _check(st, "quail_restricted_head")
 
 

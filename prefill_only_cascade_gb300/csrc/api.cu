@@ -72,6 +72,15 @@ quail_status device_state(DeviceState** out) {
   return st.status;
 }
 
+}  // namespace
+
+int quail::current_device_status() {
+  DeviceState* st = nullptr;
+  return static_cast<int>(device_state(&st));
+}
+
+namespace {
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // 3-D bf16 tensor map over [tokens, heads, d] (innermost d), 128-byte swizzle, box
@@ -326,11 +335,13 @@ quail_status quail_join_select(int32_t num_anchors, int32_t num_suffixes,
 }
 
 quail_status quail_restricted_head(int64_t n_rows, int32_t hidden, float eps, const void* h,
-                                   int64_t h_row_stride, const int32_t* row_index,
-                                   const void* gamma, const void* w8, float* logits,
-                                   int32_t* argmax, quail_stream_t stream) {
+                                   int64_t h_rows, int64_t h_row_stride,
+                                   const int32_t* row_index, const void* gamma, const void* w8,
+                                   float* logits, int32_t* argmax, quail_stream_t stream) {
   if (n_rows < 0 || hidden <= 0 || hidden % 32 != 0 || !(eps >= 0.0f) || !std::isfinite(eps))
     return QUAIL_ERR_INVALID_ARG;
+  // without a gather every output row reads the source row of the same index
+  if (h_rows < 0 || (row_index == nullptr && n_rows > h_rows)) return QUAIL_ERR_INVALID_ARG;
   if (hidden > 6144) return QUAIL_ERR_UNSUPPORTED;
   if (h_row_stride < hidden || (h_row_stride * 2) % 16 != 0) return QUAIL_ERR_INVALID_ARG;
   if (n_rows > 0) {
@@ -344,7 +355,8 @@ quail_status quail_restricted_head(int64_t n_rows, int32_t hidden, float eps, co
   DeviceState* st = nullptr;
   const quail_status ds = device_state(&st);
   if (ds != QUAIL_OK) return ds;
-  quail::HeadArgs a{n_rows, hidden, eps, h, h_row_stride, row_index, gamma, w8, logits, argmax};
+  quail::HeadArgs a{n_rows, hidden, eps, h, h_rows, h_row_stride, row_index, gamma, w8,
+                    logits, argmax, st->err_word};
   const cudaError_t e =
       quail::launch_restricted_head(a, st->num_sms, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QUAIL_OK : QUAIL_ERR_CUDA;

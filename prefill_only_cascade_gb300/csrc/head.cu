@@ -59,10 +59,10 @@ __device__ __forceinline__ float sq_sum_bf16x8(const uint4& v, float acc) {
 
 __global__ void __launch_bounds__(kHeadThreads)
 restricted_head_kernel(int64_t n_rows, int hidden, float eps, const __nv_bfloat16* __restrict__ h,
-                       int64_t stride, const int32_t* __restrict__ row_index,
+                       int64_t h_rows, int64_t stride, const int32_t* __restrict__ row_index,
                        const __nv_bfloat16* __restrict__ gamma,
                        const __nv_bfloat16* __restrict__ w8, float* __restrict__ logits,
-                       int32_t* __restrict__ argmax) {
+                       int32_t* __restrict__ argmax, unsigned* err_word) {
   extern __shared__ __align__(16) uint4 wfrag[];  // [chunks][32 lanes] hi, then the same lo
   const int nchunks = hidden / 32;
   uint4* whi = wfrag;
@@ -102,9 +102,16 @@ restricted_head_kernel(int64_t n_rows, int hidden, float eps, const __nv_bfloat1
 
   for (int64_t grp = warp0; grp < ngroups; grp += nwarps) {
     const int64_t rowA = grp * 16 + g, rowB = rowA + 8;
-    const bool okA = rowA < n_rows, okB = rowB < n_rows;
-    const int64_t srcA = okA ? (row_index ? static_cast<int64_t>(row_index[rowA]) : rowA) : 0;
-    const int64_t srcB = okB ? (row_index ? static_cast<int64_t>(row_index[rowB]) : rowB) : 0;
+    const bool outA = rowA < n_rows, outB = rowB < n_rows;  // output rows that exist
+    int64_t srcA = outA ? (row_index ? static_cast<int64_t>(row_index[rowA]) : rowA) : 0;
+    int64_t srcB = outB ? (row_index ? static_cast<int64_t>(row_index[rowB]) : rowB) : 0;
+    // a gathered source row outside h is never read: its row gets NaN logits, argmax -1
+    const bool badA = outA && (srcA < 0 || srcA >= h_rows);
+    const bool badB = outB && (srcB < 0 || srcB >= h_rows);
+    if (badA) srcA = 0;
+    if (badB) srcB = 0;
+    if ((badA || badB) && t == 0) atomicOr(err_word, kErrDeviceBounds);
+    const bool okA = outA && !badA, okB = outB && !badB;  // rows that are read
     const __nv_bfloat16* pA = h + srcA * stride + 8 * t;
     const __nv_bfloat16* pB = h + srcB * stride + 8 * t;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -171,13 +178,16 @@ restricted_head_kernel(int64_t n_rows, int hidden, float eps, const __nv_bfloat1
       if (ovA > vA || (ovA == vA && oiA < iA)) { vA = ovA; iA = oiA; }
       if (ovB > vB || (ovB == vB && oiB < iB)) { vB = ovB; iB = oiB; }
     }
-    if (okA) {
-      *reinterpret_cast<float2*>(logits + rowA * 8 + 2 * t) = make_float2(lA0, lA1);
-      if (t == 0) argmax[rowA] = iA;
+    const float nan = __int_as_float(0x7fc00000);
+    if (outA) {
+      *reinterpret_cast<float2*>(logits + rowA * 8 + 2 * t) =
+          badA ? make_float2(nan, nan) : make_float2(lA0, lA1);
+      if (t == 0) argmax[rowA] = badA ? -1 : iA;
     }
-    if (okB) {
-      *reinterpret_cast<float2*>(logits + rowB * 8 + 2 * t) = make_float2(lB0, lB1);
-      if (t == 0) argmax[rowB] = iB;
+    if (outB) {
+      *reinterpret_cast<float2*>(logits + rowB * 8 + 2 * t) =
+          badB ? make_float2(nan, nan) : make_float2(lB0, lB1);
+      if (t == 0) argmax[rowB] = badB ? -1 : iB;
     }
   }
 }
@@ -204,9 +214,9 @@ cudaError_t launch_restricted_head(const HeadArgs& a, int num_sms, cudaStream_t 
                            ? need
                            : static_cast<int64_t>(num_sms) * per_sm;
   restricted_head_kernel<<<static_cast<unsigned>(grid), kHeadThreads, smem, stream>>>(
-      a.n_rows, a.hidden, a.eps, static_cast<const __nv_bfloat16*>(a.h), a.h_row_stride,
-      a.row_index, static_cast<const __nv_bfloat16*>(a.gamma),
-      static_cast<const __nv_bfloat16*>(a.w8), a.logits, a.argmax);
+      a.n_rows, a.hidden, a.eps, static_cast<const __nv_bfloat16*>(a.h), a.h_rows,
+      a.h_row_stride, a.row_index, static_cast<const __nv_bfloat16*>(a.gamma),
+      static_cast<const __nv_bfloat16*>(a.w8), a.logits, a.argmax, a.err_word);
   return cudaGetLastError();
 }
 

@@ -7,17 +7,23 @@
 
 namespace quail {
 
+// Status (a quail_status value) of the current device for the library: QUAIL_OK on a
+// GB300 after the one-time set-up, else the same code every entry point returns.
+int current_device_status();
+
 struct HeadArgs {
   int64_t n_rows;
   int hidden;
   float eps;
   const void* h;
+  int64_t h_rows;
   int64_t h_row_stride;
   const int32_t* row_index;
   const void* gamma;
   const void* w8;
   float* logits;
   int32_t* argmax;
+  unsigned* err_word;  // the library's device error word (bounds failures)
 };
 size_t restricted_head_smem_bytes(int hidden);
 cudaError_t launch_restricted_head(const HeadArgs& a, int num_sms, cudaStream_t stream);

@@ -38,26 +38,28 @@ static_assert(kScratchBytes % 256 == 0, "scratch size must keep 256-byte alignme
 static __device__ __align__(256) unsigned char g_cascade_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
-struct ScratchAddr {
-  bool looked_up = false;
-  cudaError_t status = cudaErrorUnknown;
-  void* ptr = nullptr;
-};
 std::mutex g_scratch_mutex;
-ScratchAddr g_scratch[kMaxDevices];
+void* g_scratch[kMaxDevices];  // device address per device once a lookup has succeeded
 
-// Device address of the scratch array on the current device (looked up once per device).
+// Device address of the scratch array on the current device. The device is checked first
+// (a device other than a GB300 gets QUAIL_ERR_UNSUPPORTED, as from every entry point);
+// only a successful lookup is kept, so a failed one (for example a first call made while
+// the stream is being captured) is tried again on the next call.
 quail_status scratch_address(void** out) {
+  const quail_status dev_status = static_cast<quail_status>(quail::current_device_status());
+  if (dev_status != QUAIL_OK) return dev_status;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QUAIL_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  ScratchAddr& s = g_scratch[dev];
-  if (!s.looked_up) {
-    s.looked_up = true;
-    s.status = cudaGetSymbolAddress(&s.ptr, g_cascade_scratch);
+  if (g_scratch[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_cascade_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();  // clear the error so that later calls start clean
+      return QUAIL_ERR_CUDA;
+    }
+    g_scratch[dev] = p;
   }
-  if (s.status != cudaSuccess || s.ptr == nullptr) return QUAIL_ERR_CUDA;
-  *out = s.ptr;
+  *out = g_scratch[dev];
   return QUAIL_OK;
 }
 

@@ -106,11 +106,15 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 // Every thread of every CTA of the cluster: the cluster's shared-memory writes before it
-// are visible to all its threads after it.
+// are visible to all its threads after it. The forms without .aligned are used: .aligned
+// requires every thread of the warp to execute the barrier instruction together, which
+// the compiler does not guarantee after divergent code (a branch taken by some lanes, a
+// per-thread loop); __syncwarp() reconverges the warp first all the same.
 __device__ __forceinline__ void cluster_sync() {
+  __syncwarp();
   asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+      "barrier.cluster.arrive.release;\n\t"
+      "barrier.cluster.wait.acquire;" ::: "memory");
 }
 // Address of `p` (this CTA's shared memory) in the shared memory of cluster CTA `rank`.
 __device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {

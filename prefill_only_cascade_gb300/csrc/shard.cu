@@ -67,3 +67,64 @@ extern "C" quail_status quail_shard_anchors(int32_t num_anchors, const int32_t* 
     for (int32_t r = 0; r < num_ranks; ++r) rank_pairs[r] = load[r];
   return QUAIL_OK;
 }
+
+// One rank's sub-batch: its anchors in their original order, each with all its suffixes.
+// Offsets are rebased prefix sums of the kept lengths; rows are indices into the full
+// batch's tensors (anchor rows of k_anc / v_anc; suffix rows of q_suf / k_suf / v_suf and of
+// out / lse). Two passes: sizes, then (if the arrays are given) the arrays.
+extern "C" quail_status quail_shard_batch(
+    int32_t num_anchors, const int32_t* anchor_offsets, const int32_t* anchor_suffix_ptr,
+    const int32_t* suffix_offsets, const int32_t* rank_of_anchor, int32_t rank,
+    quail_shard_sizes* sizes, int32_t* sub_anchor_offsets, int32_t* sub_anchor_suffix_ptr,
+    int32_t* sub_suffix_offsets, int32_t* anchors, int64_t* anchor_rows, int64_t* suffix_rows) {
+  if (num_anchors < 0 || rank < 0 || sizes == nullptr) return QUAIL_ERR_INVALID_ARG;
+  if (anchor_offsets == nullptr || anchor_suffix_ptr == nullptr || suffix_offsets == nullptr ||
+      (num_anchors > 0 && rank_of_anchor == nullptr))
+    return QUAIL_ERR_INVALID_ARG;
+  if (anchor_suffix_ptr[0] != 0) return QUAIL_ERR_INVALID_ARG;
+  const bool any_out = sub_anchor_offsets || sub_anchor_suffix_ptr || sub_suffix_offsets ||
+                       anchors || anchor_rows || suffix_rows;
+  const bool all_out = sub_anchor_offsets && sub_anchor_suffix_ptr && sub_suffix_offsets &&
+                       anchors && anchor_rows && suffix_rows;
+  if (any_out && !all_out) return QUAIL_ERR_INVALID_ARG;
+  // sizes (and the same checks as quail_shard_anchors)
+  int64_t n_anchor = 0, n_suffix = 0, t_anchor = 0, t_suffix = 0;
+  for (int32_t a = 0; a < num_anchors; ++a) {
+    if (anchor_offsets[a + 1] < anchor_offsets[a] ||
+        anchor_suffix_ptr[a + 1] < anchor_suffix_ptr[a])
+      return QUAIL_ERR_INVALID_ARG;
+    for (int32_t s = anchor_suffix_ptr[a]; s < anchor_suffix_ptr[a + 1]; ++s)
+      if (suffix_offsets[s + 1] < suffix_offsets[s]) return QUAIL_ERR_INVALID_ARG;
+    if (rank_of_anchor[a] != rank) continue;
+    ++n_anchor;
+    n_suffix += anchor_suffix_ptr[a + 1] - anchor_suffix_ptr[a];
+    t_anchor += static_cast<int64_t>(anchor_offsets[a + 1]) - anchor_offsets[a];
+    t_suffix += static_cast<int64_t>(suffix_offsets[anchor_suffix_ptr[a + 1]]) -
+                suffix_offsets[anchor_suffix_ptr[a]];
+  }
+  if (t_anchor > INT32_MAX || t_suffix > INT32_MAX) return QUAIL_ERR_UNSUPPORTED;
+  sizes->num_anchors = static_cast<int32_t>(n_anchor);
+  sizes->num_suffixes = static_cast<int32_t>(n_suffix);
+  sizes->anchor_tokens = t_anchor;
+  sizes->suffix_tokens = t_suffix;
+  if (!all_out) return QUAIL_OK;
+  // arrays
+  int32_t ia = 0, is = 0;
+  int64_t ra = 0, rs = 0;
+  sub_anchor_offsets[0] = 0;
+  sub_anchor_suffix_ptr[0] = 0;
+  sub_suffix_offsets[0] = 0;
+  for (int32_t a = 0; a < num_anchors; ++a) {
+    if (rank_of_anchor[a] != rank) continue;
+    anchors[ia] = a;
+    for (int32_t r = anchor_offsets[a]; r < anchor_offsets[a + 1]; ++r) anchor_rows[ra++] = r;
+    sub_anchor_offsets[ia + 1] = static_cast<int32_t>(ra);
+    for (int32_t s = anchor_suffix_ptr[a]; s < anchor_suffix_ptr[a + 1]; ++s) {
+      for (int32_t r = suffix_offsets[s]; r < suffix_offsets[s + 1]; ++r) suffix_rows[rs++] = r;
+      sub_suffix_offsets[++is] = static_cast<int32_t>(rs);
+    }
+    sub_anchor_suffix_ptr[ia + 1] = is;
+    ++ia;
+  }
+  return QUAIL_OK;
+}

@@ -53,6 +53,20 @@ int main(void) {
   CHECK(quail_shard_anchors(3, ao, asp, so, 2, rank_of, pairs) == QUAIL_OK, "shard call");
   CHECK(rank_of[0] == 0 && rank_of[1] == 1 && rank_of[2] == 1, "shard plan");
   CHECK(pairs[0] == 19 && pairs[1] == 3, "shard loads");
+  /* rank 1's sub-batch: anchors 1 and 2 (0 and 7 tokens) with suffixes 2 (2 tokens) */
+  quail_shard_sizes sz;
+  CHECK(quail_shard_batch(3, ao, asp, so, rank_of, 1, &sz, NULL, NULL, NULL, NULL, NULL,
+                          NULL) == QUAIL_OK &&
+            sz.num_anchors == 2 && sz.num_suffixes == 1 && sz.anchor_tokens == 7 &&
+            sz.suffix_tokens == 2,
+        "sub-batch sizes");
+  int32_t sao[3], sasp[3], sso[2], anc[2];
+  int64_t arows[7], srows[2];
+  CHECK(quail_shard_batch(3, ao, asp, so, rank_of, 1, &sz, sao, sasp, sso, anc, arows,
+                          srows) == QUAIL_OK &&
+            sao[1] == 0 && sao[2] == 7 && sasp[1] == 1 && sasp[2] == 1 && sso[1] == 2 &&
+            anc[0] == 1 && anc[1] == 2 && arows[0] == 3 && srows[0] == 4 && srows[1] == 5,
+        "sub-batch arrays");
 
   /* cache plan: anchors of 4, 4 and 2 tokens, capacity 8, accesses 0 1 2 0 1 */
   const int64_t size[3] = {4, 4, 2};

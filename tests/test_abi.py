@@ -109,8 +109,9 @@ def test_cascade_rejects_bad_pointers():
 
 def test_head_rejects_bad_arguments():
     f = ctypes.c_void_p(0x10000)
-    call = lambda n, hid, eps=1e-6, stride=None, h=f, lg=f: q.lib.quail_restricted_head(
-        n, hid, eps, h, hid if stride is None else stride, None, f, f, lg, f, None)
+    call = lambda n, hid, eps=1e-6, stride=None, h=f, lg=f, rows=4, idx=None: \
+        q.lib.quail_restricted_head(n, hid, eps, h, rows, hid if stride is None else stride,
+                                    idx, f, f, lg, f, None)
     assert call(-1, 256) == q.QUAIL_ERR_INVALID_ARG
     assert call(4, 250) == q.QUAIL_ERR_INVALID_ARG            # not a multiple of 32
     assert call(4, 256, eps=-1.0) == q.QUAIL_ERR_INVALID_ARG
@@ -119,6 +120,10 @@ def test_head_rejects_bad_arguments():
     assert call(4, 256, h=None) == q.QUAIL_ERR_INVALID_ARG
     assert call(4, 256, lg=ctypes.c_void_p(0x10004)) == q.QUAIL_ERR_INVALID_ARG
     assert call(4, 8192) == q.QUAIL_ERR_UNSUPPORTED
+    assert call(4, 256, rows=3) == q.QUAIL_ERR_INVALID_ARG   # more output rows than h has
+    assert call(4, 256, rows=-1) == q.QUAIL_ERR_INVALID_ARG
+    # with a gather the row count of h only bounds the indices (checked on the device)
+    assert call(4, 256, rows=3, idx=ctypes.c_void_p(0x10002)) == q.QUAIL_ERR_INVALID_ARG
 
 
 def test_quantize_rejects_bad_arguments():

@@ -136,6 +136,26 @@ def test_head_tiny_every_row_and_gather():
     check_head(x["h"], x["gamma"], x["w8"], cfg.eps, lg2, am2, row_index=idx)
 
 
+def test_head_out_of_range_gather_index_is_reported_not_read():
+    # indices -1 and h_rows are checked on the device: those rows get NaN logits and
+    # argmax -1 and the call reports QUAIL_ERR_DEVICE_BOUNDS; the other rows are exact
+    import prefill_only_cascade_gb300 as q
+    cfg = workloads.HEAD_CONFIGS["tiny"]
+    x = workloads.make_head_inputs(cfg, "cuda", num_rows=100)
+    idx = torch.tensor([0, 5, -1, 99, 100, 7, 2**31 - 1, 42], dtype=torch.int32, device="cuda")
+    logits = torch.zeros(8, 8, dtype=torch.float32, device="cuda")
+    am = torch.zeros(8, dtype=torch.int32, device="cuda")
+    q.restricted_head(x["h"], x["gamma"], x["w8"], logits, am, eps=cfg.eps, row_index=idx)
+    assert q.get_device_error() == q.QUAIL_ERR_DEVICE_BOUNDS
+    assert q.get_device_error() == q.QUAIL_OK          # reading the word clears it
+    bad = np.array([False, False, True, False, True, False, True, False])
+    lg, a = logits.cpu().numpy(), am.cpu().numpy()
+    assert np.isnan(lg[bad]).all() and (a[bad] == -1).all()
+    good = torch.from_numpy(np.flatnonzero(~bad)).cuda()
+    check_head(x["h"], x["gamma"], x["w8"], cfg.eps, logits[good], am[good],
+               row_index=idx[good])
+
+
 def test_head_ragged_row_count_and_strided_rows():
     import prefill_only_cascade_gb300 as q
     g = torch.Generator(device="cuda").manual_seed(5)

@@ -1,7 +1,8 @@
-"""The N>1 path on CPU with two gloo ranks. bench.py: each rank runs its own batch of the
-same shape (weak scaling), only the barrier and the max-over-ranks of the timing cross
-ranks. One batch split by anchor (quail_shard_anchors + shard_batch): the ranks' results
-reassemble the full batch's result; only results are gathered."""
+"""The N>1 path on CPU with two gloo ranks. bench.py: the job's anchors are split over the
+ranks by quail_shard_anchors / quail_shard_batch (N batches for weak scaling, one for
+strong); only the barrier and the max-over-ranks of the timing cross ranks. One batch
+split by anchor: the ranks' results reassemble the full batch's result; only results are
+gathered."""
 import os
 import socket
 
@@ -30,25 +31,36 @@ def _worker(rank, world, port, out):
         got = bench.max_over_ranks(world, float(10 + 5 * rank), device="cpu")
         total = bench.sum_over_ranks(world, float(1 + rank), device="cpu")
         assert total == 3.0
-        cfg = bench.rank_workload(workloads.ATTN_CONFIGS["tiny"], rank)
-        lay = workloads.make_layout(cfg)
-        t = workloads.make_attention_inputs(cfg, lay, "cpu")
-        out[rank] = (got, cfg.seed, float(t["q_suf"].float().sum()), lay.total_suffix_tokens)
+        cfg = workloads.ATTN_CONFIGS["ragged"]
+        weak, plan = bench.rank_layout(cfg, world, rank)
+        strong, _ = bench.rank_layout(cfg, world, rank, strong=True)
+        tok = bench.sum_over_ranks(world, float(weak.total_suffix_tokens), device="cpu")
+        out[rank] = (got, plan, weak.num_anchors, weak.total_suffix_tokens, tok,
+                     strong.num_anchors, strong.total_suffix_tokens)
         bench.barrier(world)
     finally:
         dist.destroy_process_group()
 
 
-def test_two_gloo_ranks_max_timing_and_distinct_batches():
+def test_two_gloo_ranks_max_timing_and_anchor_shards():
     world = 2
     mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.start_processes(_worker, args=(world, _free_port(), out), nprocs=world,
                        start_method="spawn", join=True)
     assert out[0][0] == out[1][0] == 15.0          # max over ranks
-    assert out[0][1] != out[1][1]                  # rank-specific seeds
-    assert out[0][2] != out[1][2]                  # so different data
-    assert out[0][3] == out[1][3]                  # of the same shape (weak scaling)
+    assert out[0][1] == out[1][1]                  # every rank derives the same plan
+    cfg = workloads.ATTN_CONFIGS["ragged"]
+    one = workloads.make_layout(cfg)
+    # weak scaling: the job is two batches of the workload's shape, split by anchor
+    assert out[0][2] + out[1][2] == 2 * cfg.num_anchors
+    assert out[0][4] == bench.global_layout(cfg, 2).total_suffix_tokens
+    assert abs(out[0][3] - out[1][3]) < 0.02 * out[0][3]   # balanced ranks
+    # strong scaling: one batch split in two
+    assert out[0][5] + out[1][5] == cfg.num_anchors
+    assert out[0][6] + out[1][6] == one.total_suffix_tokens
+    loads = out[0][1]["rank_pairs"]
+    assert max(loads) <= 1.01 * sum(loads) / 2
 
 
 def _shard_worker(rank, world, port, out):

@@ -68,3 +68,41 @@ def test_special_cases():
     # equal costs: round robin in index order
     assert shard.lpt([4] * 7, 3)[0] == [0, 1, 2, 0, 1, 2, 0]
     assert shard.lpt([], 2) == ([], [0, 0])
+
+
+def test_sub_batch_hand_worked_and_partition():
+    # anchors of 3, 0 and 2 tokens with 2, 1 and 1 suffixes of 1, 2, 0 and 4 tokens;
+    # anchors 0 and 2 on rank 1
+    ao, asp, so = [0, 3, 3, 5], [0, 2, 3, 4], [0, 1, 3, 3, 7]
+    r1 = shard.sub_batch(ao, asp, so, [1, 0, 1], 1)
+    assert r1 == {"anchor_offsets": [0, 3, 5], "anchor_suffix_ptr": [0, 2, 3],
+                  "suffix_offsets": [0, 1, 3, 7], "anchors": [0, 2],
+                  "anchor_rows": [0, 1, 2, 3, 4], "suffix_rows": [0, 1, 2, 3, 4, 5, 6]}
+    r0 = shard.sub_batch(ao, asp, so, [1, 0, 1], 0)
+    assert r0 == {"anchor_offsets": [0, 0], "anchor_suffix_ptr": [0, 1],
+                  "suffix_offsets": [0, 0], "anchors": [1], "anchor_rows": [],
+                  "suffix_rows": []}
+    # random plans: the sub-batches partition the rows and keep every length
+    rng = np.random.default_rng(12)
+    for _ in range(30):
+        A = int(rng.integers(1, 7))
+        counts = rng.integers(0, 4, size=A)
+        lay = workloads.layout_from_lengths(rng.integers(0, 20, size=A), counts,
+                                            rng.integers(0, 9, size=int(counts.sum())))
+        R = int(rng.integers(1, 4))
+        rank_of = [int(x) for x in rng.integers(0, R, size=A)]
+        a_rows, s_rows, anchors = [], [], []
+        for r in range(R):
+            sb = shard.sub_batch(lay.anchor_offsets, lay.anchor_suffix_ptr,
+                                 lay.suffix_offsets, rank_of, r)
+            a_rows += sb["anchor_rows"]
+            s_rows += sb["suffix_rows"]
+            anchors += sb["anchors"]
+            la = np.diff(sb["anchor_offsets"])
+            assert list(la) == [int(lay.anchor_lens[a]) for a in sb["anchors"]]
+            ls = np.diff(sb["suffix_offsets"])
+            assert list(ls) == [int(x) for a in sb["anchors"]
+                                for x in lay.suffix_lens[lay.suffix_anchor == a]]
+        assert sorted(a_rows) == list(range(lay.total_anchor_tokens))
+        assert sorted(s_rows) == list(range(lay.total_suffix_tokens))
+        assert sorted(anchors) == list(range(A))

@@ -92,3 +92,41 @@ def test_sub_batches_reproduce_the_full_batch():
     assert np.array_equal(np.sort(rows), np.arange(T_S))      # every row exactly once
     np.testing.assert_allclose(out, ref_out, rtol=0, atol=1e-12)
     np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=1e-12)
+
+
+def test_sub_batch_matches_the_oracle_bit_for_bit():
+    rng = np.random.default_rng(31)
+    for trial in range(40):
+        lay = _random_layout(rng)
+        ranks = int(rng.integers(1, 5))
+        rank_of, _ = q.shard_anchors(lay.anchor_offsets, lay.anchor_suffix_ptr,
+                                     lay.suffix_offsets, ranks)
+        for r in range(ranks + 1):            # rank == ranks owns nothing: an empty batch
+            got = q.shard_batch(lay.anchor_offsets, lay.anchor_suffix_ptr, lay.suffix_offsets,
+                                rank_of, r)
+            ref = shard.sub_batch(lay.anchor_offsets, lay.anchor_suffix_ptr,
+                                  lay.suffix_offsets, rank_of, r)
+            for key, val in ref.items():
+                assert got[key].tolist() == val, (trial, r, key)
+
+
+def test_sub_batch_rejects_bad_arguments():
+    import ctypes
+    ao = np.array([0, 3, 5], np.int32)
+    asp = np.array([0, 1, 2], np.int32)
+    so = np.array([0, 2, 4], np.int32)
+    ro = np.array([0, 1], np.int32)
+    sz = q.ShardSizes()
+    p = lambda x: x.ctypes.data
+    call = lambda A=2, ao=ao, asp=asp, so=so, ro=ro, rank=0, sizes=ctypes.byref(sz), arrays=(
+        None,) * 6: q.lib.quail_shard_batch(A, p(ao), p(asp), p(so), p(ro), rank, sizes, *arrays)
+    assert call() == q.QUAIL_OK and (sz.num_anchors, sz.num_suffixes) == (1, 1)
+    assert (sz.anchor_tokens, sz.suffix_tokens) == (3, 2)
+    assert call(rank=-1) == q.QUAIL_ERR_INVALID_ARG
+    assert call(A=-1) == q.QUAIL_ERR_INVALID_ARG
+    assert call(sizes=None) == q.QUAIL_ERR_INVALID_ARG
+    assert call(ao=np.array([0, 3, 2], np.int32)) == q.QUAIL_ERR_INVALID_ARG   # length < 0
+    assert call(asp=np.array([1, 1, 2], np.int32)) == q.QUAIL_ERR_INVALID_ARG  # CSR not from 0
+    buf = np.zeros(8, np.int64)
+    # some output arrays given, others not
+    assert call(arrays=(p(buf), None, None, None, None, None)) == q.QUAIL_ERR_INVALID_ARG
