@@ -12,6 +12,8 @@ Prints ONE JSON line (metric: suffix tokens per second). The line also carries, 
 in the same process after the headline: `sub.join` (the Qwen3-4B join), `sub.fp8_long`
 (e4m3 anchor KV), `sub.head` (2 M head rows) and `sub.softmax_stress` (the join with
 queries scaled x4 and x8), each with its own roofline, oracle baseline and parity.
+Each attention workload also carries `fused_vs_two_pass`: the same batch through the
+two-pass entry point (anchor pass, suffix pass, LSE merge) timed against the fused call.
 `--impl reference` times the float64 CPU oracle on a bounded sample of the same workload.
 """
 from __future__ import annotations
@@ -430,8 +432,50 @@ def redo_items(ws) -> int:
     return int(ws[4:8].view(torch.int32).item())
 
 
+def compare_two_pass(q, desc, t, out, lse, k_scale, v_scale, fused_ms, steps, stream,
+                     parity_refs=None):
+    """The same batch through quail_cascade_attn_two_pass (anchor pass, suffix pass, LSE
+    merge) with the merge in the suffix pass's epilogue and as its own kernel: mean call
+    time of each (CUDA events) against the fused call, and parity of each on the sampled
+    suffixes. Writes its results into out / lse (after the fused call's parity was taken)."""
+    ws2 = torch.empty(q.cascade_two_pass_workspace_size(desc), dtype=torch.uint8,
+                      device=out.device)
+    res = {"fused_ms": round(fused_ms, 4)}
+    for merge, key in ((True, "merge_in_suffix_pass"), (False, "merge_kernel")):
+        run = lambda: q.cascade_attn_two_pass(
+            desc, t["q_suf"], t["k_anc"], t["v_anc"], t["k_suf"], t["v_suf"],
+            t["anchor_offsets"], t["anchor_suffix_ptr"], t["suffix_offsets"], out, lse, ws2,
+            k_scale, v_scale, merge_in_suffix_pass=merge, stream=stream)
+        for _ in range(2):
+            run()
+        torch.cuda.synchronize()
+        evs = _events(steps)
+        for a, b in evs:
+            a.record(stream)
+            run()
+            b.record(stream)
+        torch.cuda.synchronize()
+        if q.get_device_error() != q.QUAIL_OK:
+            raise RuntimeError("device error in the two-pass run")
+        entry = {"ms": round(statistics.mean(a.elapsed_time(b) for a, b in evs), 4)}
+        entry["vs_fused"] = round(entry["ms"] / fused_ms, 4)
+        if parity_refs:
+            entry["parity"] = sampled_parity(parity_refs, out, lse)
+        res[key] = entry
+    best = min(("fused", fused_ms), ("two_pass_merge_in_suffix_pass",
+                                     res["merge_in_suffix_pass"]["ms"]),
+               ("two_pass_merge_kernel", res["merge_kernel"]["ms"]), key=lambda x: x[1])
+    res["faster"] = best[0]
+    res["launches"] = {"fused": "3 schedule + fast + exact",
+                       "two_pass": "fill + 2 x (3 schedule + fast + exact) (+ merge kernel)"}
+    res["workspace_bytes"] = int(ws2.numel())
+    del ws2
+    torch.cuda.empty_cache()
+    return res
+
+
 def measure_attention(q, cfg, layout, dev, args, *, steps, e2e=False, cpu_budget=15.0,
-                      world=1, rank=0, scaling="weak", fp8_diagnostic=False):
+                      world=1, rank=0, scaling="weak", fp8_diagnostic=False, two_pass=False):
     """One attention workload: cascade attention over the whole batch then the restricted
     head on the last token of every suffix, `steps` times on resident inputs. Returns the
     measurement dict (the headline line's keys, or a sub-object)."""
@@ -540,10 +584,10 @@ def measure_attention(q, cfg, layout, dev, args, *, steps, e2e=False, cpu_budget
            "gpu_launches": (7 if kv_fp8 and layout.total_anchor_tokens > 0 else 6) * steps,
            "clocks": clk.summary()}
 
+    parity_refs = {}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         def host_cases(ids):
             return workloads.gather_suffix_case(t_bf16, layout, ids)
-        parity_refs = {}
         v, cores, sample, dt = cpu_oracle_sample(
             layout, cfg, host_cases, budget_s=cpu_budget,
             kv_for=fp8_oracle_kv(t_bf16, layout) if kv_fp8 else None, results=parity_refs)
@@ -559,6 +603,10 @@ def measure_attention(q, cfg, layout, dev, args, *, steps, e2e=False, cpu_budget
             cpu_oracle_sample(layout, cfg, host_cases, budget_s=min(cpu_budget, 6.0),
                               max_suffixes=64, results=diag, with_head=False)
             res["diagnostic_vs_unquantised"] = sampled_parity(diag, out, lse)
+    if two_pass:
+        res["fused_vs_two_pass"] = compare_two_pass(
+            q, desc, t, out, lse, k_scale, v_scale, attn_ms, max(3, min(steps, 5)), stream,
+            parity_refs)
     if e2e:
         res["e2e"] = run_e2e_chunked(q, cfg, layout, t, hx["h"], last, k_scale, v_scale, dev,
                                      stream, world, steps=max(3, min(steps, 6)))
@@ -768,6 +816,12 @@ def measure_softmax_stress(q, args, dev, scales=(4.0, 8.0)):
     pk, src = peaks()
     flops = attention_flops(layout, hq, d)
     items = work_items(layout, hkv, hq // hkv)
+    # Bound for these peaked rows: the bf16 bounds, plus one bf16 rounding (2^-9
+    # relative) of the largest |V|: the output is close to one V row, and the fast
+    # kernel's P of that row is 2^(s c - m_ref) rounded to bf16 whenever the row max lies
+    # past the first key tile (the same derivation as the FP8 path's bound).
+    vmax = float(max(t["v_anc"].abs().max(), t["v_suf"].abs().max()))
+    bound = {"max_abs": 2e-2 + vmax * 2.0 ** -9, "rel_l2": 5e-3, "lse_abs": 1e-3}
     res = {}
     for s in (1.0,) + tuple(scales):
         qs = t["q_suf"] * s
@@ -794,7 +848,12 @@ def measure_softmax_stress(q, args, dev, scales=(4.0, 8.0)):
             cpu_oracle_sample(layout, cfg, lambda ids: workloads.gather_suffix_case(t, layout, ids),
                               budget_s=3.0, max_suffixes=48, with_head=False, results=refs,
                               q_scale=s)
-            entry["parity"] = sampled_parity(refs, out, lse)
+            par = sampled_parity(refs, out, lse)
+            par["bound"] = bound
+            par["within_bound"] = ("max_abs" in par and par["max_abs"] <= bound["max_abs"] and
+                                   par["rel_l2"] <= bound["rel_l2"] and
+                                   par["lse_abs"] <= bound["lse_abs"])
+            entry["parity"] = par
         res[f"x{s:g}"] = entry
         del qs
     del t, ws, out, lse
@@ -940,7 +999,8 @@ def run_ours(args):
     layout, shard_plan = rank_layout(cfg, world, rank, strong=args.strong)
     cfg_rank = dataclasses.replace(cfg, seed=cfg.seed + 7919 * rank) if rank else cfg
     head = measure_attention(q, cfg_rank, layout, dev, args, steps=args.steps,
-                             e2e=not args.no_e2e, world=world, rank=rank, scaling=scaling)
+                             e2e=not args.no_e2e, world=world, rank=rank, scaling=scaling,
+                             two_pass=(world == 1 and not args.no_sub))
     line = {"metric": METRIC, "value": head.pop("value"), "unit": head.pop("unit"),
             "n_gpus": world, "steps": head.pop("steps"), "warmup": head.pop("warmup"),
             "ms_per_step": head.pop("ms_per_step"), "higher_is_better": True,
@@ -958,7 +1018,7 @@ def run_ours(args):
             c = _attn_cfg(args, name)
             sub[name] = measure_attention(q, c, workloads.make_layout(c), dev, args,
                                           steps=sub_steps, cpu_budget=budget,
-                                          fp8_diagnostic=(name == "fp8_long"))
+                                          fp8_diagnostic=(name == "fp8_long"), two_pass=True)
         sub["head"] = measure_bandwidth_kernel(q, args, "head", sub_steps)
         sub["softmax_stress"] = measure_softmax_stress(q, args, dev)
         line["sub"] = sub

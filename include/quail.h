@@ -107,6 +107,35 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
 size_t quail_cascade_workspace_size(const quail_cascade_desc* desc);
 
 /*
+ * The same result as quail_cascade_attn computed as two passes and a merge, the three
+ * steps of [P1]'s cascade-attention bullet run apart: (A2) an anchor pass - every suffix
+ * token against its anchor's keys only - writes the normalised fp32 partial O_a and its
+ * lse_a into the workspace; (A3) a suffix pass attends causally over the suffix's own
+ * keys; (A4) the LSE merge lse = log(e^lse_a + e^lse_s), out = e^(lse_a - lse) O_a +
+ * e^(lse_s - lse) O_s, done in the suffix pass's epilogue (merge_in_suffix_pass = 1) or by
+ * a separate merge kernel over out in place (0; the suffix pass then writes O_s to out in
+ * bf16 and lse_s to the workspace). It exists to compare with the fused kernel by
+ * measurement; results agree with quail_cascade_attn within the bf16 bounds, not bit for
+ * bit (O_s or the merge add a rounding).
+ *
+ * Arguments, layouts, limits and errors as quail_cascade_attn, plus merge_in_suffix_pass
+ * (0 or 1) and a workspace of at least quail_cascade_two_pass_workspace_size(desc) bytes
+ * (the cascade's workspace + 4 * T_S * Hq * (d + 2) bytes), 16-byte aligned.
+ */
+quail_status quail_cascade_attn_two_pass(const quail_cascade_desc* desc, const void* q_suf,
+                                         const void* k_anc, const void* v_anc,
+                                         const void* k_suf, const void* v_suf,
+                                         const int32_t* anchor_offsets,
+                                         const int32_t* anchor_suffix_ptr,
+                                         const int32_t* suffix_offsets, const float* k_scale,
+                                         const float* v_scale, int32_t merge_in_suffix_pass,
+                                         void* out, float* lse, void* workspace,
+                                         size_t workspace_bytes, quail_stream_t stream);
+
+/* Workspace bytes that quail_cascade_attn_two_pass needs for `desc` (0 when invalid). */
+size_t quail_cascade_two_pass_workspace_size(const quail_cascade_desc* desc);
+
+/*
  * Causal self-attention over packed sequences: the anchors' own prefill, the step before
  * the cascade ([P1] "Como funciona", cascade-attention bullet: the shared anchor is
  * processed once and its KV reused by every suffix). For sequence s, token i and q-head h
@@ -118,6 +147,10 @@ size_t quail_cascade_workspace_size(const quail_cascade_desc* desc);
  *   seq_offsets [S+1] int32 token prefix sums (monotone, seq_offsets[S] == T, every
  *                    length <= max_seq_len; checked on the device as for the cascade)
  *   out [T, Hq, d] bf16, 32-byte aligned; lse [T, Hq] fp32 natural log, may be NULL
+ *   k_amax, v_amax [S, Hkv] fp32 out, both NULL or both given: max |k| and max |v| over
+ *                    each sequence's tokens and all d, per KV head - the inputs of
+ *                    quail_quantize_kv_fp8_with_scales. They come from the K/V tiles the
+ *                    attention already loads (no extra read of k and v).
  *   softmax_scale: 0 => 1/sqrt(d)
  *   workspace: at least quail_causal_prefill_workspace_size(...) bytes, 256-byte aligned;
  *              overwritten (the call writes two 2-entry index arrays at its start).
@@ -128,7 +161,8 @@ quail_status quail_causal_prefill_attn(int32_t num_seqs, int64_t total_tokens,
                                        int32_t num_kv_heads, int32_t head_dim,
                                        float softmax_scale, const void* q, const void* k,
                                        const void* v, const int32_t* seq_offsets, void* out,
-                                       float* lse, void* workspace, size_t workspace_bytes,
+                                       float* lse, float* k_amax, float* v_amax,
+                                       void* workspace, size_t workspace_bytes,
                                        quail_stream_t stream);
 
 /* Workspace bytes for quail_causal_prefill_attn (0 if the sizes are invalid). */
@@ -308,12 +342,33 @@ quail_status quail_restricted_head(int64_t n_rows, int32_t hidden, float eps, co
  *   and all d; code = e4m3(x / scale), x / scale rounded to fp32 first, then rounded to
  *   nearest even with saturation at +-448 (sign kept).
  *   kv_bf16 [T_A, Hkv, d] bf16 in; kv_e4m3 [T_A, Hkv, d] codes out; scale [A, Hkv] fp32
- *   out. d in {64, 128}, Hkv * d <= 4096. One kernel (clusters of CTAs) on `stream`.
+ *   out. d in {64, 128}, Hkv * d <= 4096. One kernel on `stream` (clusters of 8 CTAs
+ *   holding each (anchor, KV head) slab in shared memory: one read of kv_bf16 for
+ *   anchors up to 6,144 tokens at d = 128, two reads above). Offsets are clamped into
+ *   [0, T_A] on the device, so inconsistent ones cannot address outside the tensors.
  */
 quail_status quail_quantize_kv_fp8(int32_t num_anchors, const int32_t* anchor_offsets,
                                    int64_t total_anchor_tokens, int32_t num_kv_heads,
                                    int32_t head_dim, const void* kv_bf16, void* kv_e4m3,
                                    float* scale, quail_stream_t stream);
+
+/*
+ * The same codes and scales as quail_quantize_kv_fp8 when the max |x| of every (anchor,
+ * KV head) is already known - e.g. the k_amax / v_amax that quail_causal_prefill_attn
+ * emits while it streams the anchors' K/V ([P1] "Como funciona": the anchor is prefilled
+ * once and its KV reused), so quantising costs one read of kv_bf16 and one write.
+ *   amax [A, Hkv] fp32 (device); scale[a, g] = amax[a, g] / 448 (1 when 0) is written.
+ * Other arguments, limits and errors as quail_quantize_kv_fp8 (plus NULL or misaligned
+ * amax -> QUAIL_ERR_INVALID_ARG). The anchors' offsets must be monotone (each token row
+ * takes the scale of the anchor holding it).
+ */
+quail_status quail_quantize_kv_fp8_with_scales(int32_t num_anchors,
+                                               const int32_t* anchor_offsets,
+                                               int64_t total_anchor_tokens,
+                                               int32_t num_kv_heads, int32_t head_dim,
+                                               const void* kv_bf16, const float* amax,
+                                               void* kv_e4m3, float* scale,
+                                               quail_stream_t stream);
 
 /* Static, NUL-terminated name of a status code. */
 const char* quail_status_string(quail_status status);

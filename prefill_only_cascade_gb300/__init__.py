@@ -34,6 +34,8 @@ EXPORTED_SYMBOLS = (
     "quail_cascade_attn_noalloc", "quail_causal_prefill_attn",
     "quail_causal_prefill_workspace_size", "quail_kv_plan", "quail_shard_anchors",
     "quail_join_select", "quail_join_select_workspace_size", "quail_shard_batch",
+    "quail_cascade_attn_two_pass", "quail_cascade_two_pass_workspace_size",
+    "quail_quantize_kv_fp8_with_scales",
 )
 
 
@@ -88,6 +90,13 @@ def _load():
     lib.quail_cascade_attn_noalloc.restype = ctypes.c_int
     lib.quail_cascade_workspace_size.argtypes = [ctypes.POINTER(CascadeDesc)]
     lib.quail_cascade_workspace_size.restype = ctypes.c_size_t
+    lib.quail_cascade_attn_two_pass.argtypes = [ctypes.POINTER(CascadeDesc), vp, vp, vp, vp,
+                                                vp, i32p, i32p, i32p, f32p, f32p,
+                                                ctypes.c_int32, vp, f32p, vp, ctypes.c_size_t,
+                                                vp]
+    lib.quail_cascade_attn_two_pass.restype = ctypes.c_int
+    lib.quail_cascade_two_pass_workspace_size.argtypes = [ctypes.POINTER(CascadeDesc)]
+    lib.quail_cascade_two_pass_workspace_size.restype = ctypes.c_size_t
     lib.quail_restricted_head.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_float, vp,
                                           ctypes.c_int64, ctypes.c_int64, i32p, vp, vp, f32p,
                                           i32p, vp]
@@ -95,6 +104,10 @@ def _load():
     lib.quail_quantize_kv_fp8.argtypes = [ctypes.c_int32, i32p, ctypes.c_int64, ctypes.c_int32,
                                           ctypes.c_int32, vp, vp, f32p, vp]
     lib.quail_quantize_kv_fp8.restype = ctypes.c_int
+    lib.quail_quantize_kv_fp8_with_scales.argtypes = [ctypes.c_int32, i32p, ctypes.c_int64,
+                                                      ctypes.c_int32, ctypes.c_int32, vp, f32p,
+                                                      vp, f32p, vp]
+    lib.quail_quantize_kv_fp8_with_scales.restype = ctypes.c_int
     lib.quail_status_string.argtypes = [ctypes.c_int]
     lib.quail_status_string.restype = ctypes.c_char_p
     lib.quail_get_device_error.argtypes = [vp]
@@ -107,7 +120,8 @@ def _load():
     lib.quail_version.restype = ctypes.c_char_p
     i32, i64 = ctypes.c_int32, ctypes.c_int64
     lib.quail_causal_prefill_attn.argtypes = [i32, i64, i32, i32, i32, i32, ctypes.c_float, vp,
-                                              vp, vp, i32p, vp, f32p, vp, ctypes.c_size_t, vp]
+                                              vp, vp, i32p, vp, f32p, f32p, f32p, vp,
+                                              ctypes.c_size_t, vp]
     lib.quail_causal_prefill_attn.restype = ctypes.c_int
     lib.quail_causal_prefill_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32]
     lib.quail_causal_prefill_workspace_size.restype = ctypes.c_size_t
@@ -179,6 +193,26 @@ def cascade_attn(desc: CascadeDesc, q_suf, k_anc, v_anc, k_suf, v_suf, anchor_of
     _check(st, "quail_cascade_attn")
 
 
+def cascade_two_pass_workspace_size(desc: CascadeDesc) -> int:
+    return int(lib.quail_cascade_two_pass_workspace_size(ctypes.byref(desc)))
+
+
+def cascade_attn_two_pass(desc: CascadeDesc, q_suf, k_anc, v_anc, k_suf, v_suf,
+                          anchor_offsets, anchor_suffix_ptr, suffix_offsets, out, lse=None,
+                          workspace=None, k_scale=None, v_scale=None, merge_in_suffix_pass=True,
+                          stream=None):
+    """quail_cascade_attn_two_pass: anchor pass, suffix pass and LSE merge run apart
+    (workspace size: cascade_two_pass_workspace_size(desc))."""
+    if workspace is None:
+        raise ValueError("workspace is required (size: cascade_two_pass_workspace_size(desc))")
+    st = lib.quail_cascade_attn_two_pass(
+        ctypes.byref(desc), _ptr(q_suf), _ptr(k_anc), _ptr(v_anc), _ptr(k_suf), _ptr(v_suf),
+        _ptr(anchor_offsets), _ptr(anchor_suffix_ptr), _ptr(suffix_offsets), _ptr(k_scale),
+        _ptr(v_scale), 1 if merge_in_suffix_pass else 0, _ptr(out), _ptr(lse), _ptr(workspace),
+        ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(stream))
+    _check(st, "quail_cascade_attn_two_pass")
+
+
 def cascade_attn_noalloc(desc: CascadeDesc, q_suf, k_anc, v_anc, k_suf, v_suf, anchor_offsets,
                          anchor_suffix_ptr, suffix_offsets, out, lse=None, k_scale=None,
                          v_scale=None, stream=None):
@@ -200,15 +234,16 @@ def causal_prefill_workspace_size(num_seqs, total_tokens, max_seq_len, num_q_hea
 
 
 def causal_prefill_attn(q, k, v, seq_offsets, out, max_seq_len, lse=None, workspace=None,
-                        softmax_scale=0.0, stream=None):
+                        softmax_scale=0.0, k_amax=None, v_amax=None, stream=None):
     """quail_causal_prefill_attn: causal self-attention over packed sequences
-    (q [T, Hq, d], k/v [T, Hkv, d] bf16, seq_offsets [S+1] int32 on the device)."""
+    (q [T, Hq, d], k/v [T, Hkv, d] bf16, seq_offsets [S+1] int32 on the device); with
+    k_amax / v_amax ([S, Hkv] fp32) also the max |k| and |v| per (sequence, KV head)."""
     if workspace is None:
         raise ValueError("workspace is required (size: causal_prefill_workspace_size(...))")
     st = lib.quail_causal_prefill_attn(
         int(seq_offsets.numel() - 1), int(q.shape[0]), int(max_seq_len), int(q.shape[1]),
         int(k.shape[1]), int(q.shape[2]), float(softmax_scale), _ptr(q), _ptr(k), _ptr(v),
-        _ptr(seq_offsets), _ptr(out), _ptr(lse), _ptr(workspace),
+        _ptr(seq_offsets), _ptr(out), _ptr(lse), _ptr(k_amax), _ptr(v_amax), _ptr(workspace),
         ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(stream))
     _check(st, "quail_causal_prefill_attn")
 
@@ -308,6 +343,16 @@ def quantize_kv_fp8(kv_bf16, anchor_offsets, codes, scale, stream=None):
                                    int(hkv), int(d), _ptr(kv_bf16), _ptr(codes), _ptr(scale),
                                    _stream(stream))
     _check(st, "quail_quantize_kv_fp8")
+
+
+def quantize_kv_fp8_with_scales(kv_bf16, anchor_offsets, amax, codes, scale, stream=None):
+    """quail_quantize_kv_fp8_with_scales: the same codes and scales given the max |x| of
+    every (anchor, KV head) (e.g. the causal prefill's k_amax / v_amax)."""
+    T, hkv, d = kv_bf16.shape
+    st = lib.quail_quantize_kv_fp8_with_scales(
+        int(anchor_offsets.numel() - 1), _ptr(anchor_offsets), int(T), int(hkv), int(d),
+        _ptr(kv_bf16), _ptr(amax), _ptr(codes), _ptr(scale), _stream(stream))
+    _check(st, "quail_quantize_kv_fp8_with_scales")
 
 
 def get_device_error(stream=None) -> int:

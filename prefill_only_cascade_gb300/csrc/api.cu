@@ -168,14 +168,22 @@ quail_status quail_get_device_error(quail_stream_t stream) {
   return QUAIL_ERR_DEVICE_BOUNDS;
 }
 
-quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_suf,
-                                const void* k_anc, const void* v_anc, const void* k_suf,
-                                const void* v_suf, const int32_t* anchor_offsets,
-                                const int32_t* anchor_suffix_ptr,
-                                const int32_t* suffix_offsets, const float* k_scale,
-                                const float* v_scale, void* out, float* lse,
-                                void* workspace, size_t workspace_bytes,
-                                quail_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Validation of one cascade call and the kernels' parameters. `extra_bytes` is workspace
+// that the caller's variant needs after the cascade's own (256-byte aligned start).
+// Returns QUAIL_OK with *nothing = true when there is no work (T_S = 0).
+quail_status prepare_cascade(const quail_cascade_desc* desc, const void* q_suf, const void* k_anc,
+                             const void* v_anc, const void* k_suf, const void* v_suf,
+                             const int32_t* anchor_offsets, const int32_t* anchor_suffix_ptr,
+                             const int32_t* suffix_offsets, const float* k_scale,
+                             const float* v_scale, void* out, float* lse, void* workspace,
+                             size_t workspace_bytes, size_t extra_bytes, quail::CascadeParams* pp,
+                             quail::CascadeMaps* mp, DeviceState** stp, size_t* ws_used,
+                             bool* nothing) {
+  *nothing = false;
   if (desc == nullptr) return QUAIL_ERR_INVALID_ARG;
   const quail_cascade_desc& d = *desc;
   const int64_t kMaxTok = (1ll << 31) - 1;
@@ -219,17 +227,22 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
   if (item_bound > (1ll << 31) - 1) return QUAIL_ERR_UNSUPPORTED;
   const quail::CascadeWorkspace wl = quail::cascade_workspace_layout(
       d.num_anchors, d.total_suffix_tokens, item_bound, anchor_bf16_bytes(d));
-  if (workspace == nullptr || workspace_bytes < wl.total || !aligned16(workspace))
+  *ws_used = wl.total;
+  if (workspace == nullptr || workspace_bytes < wl.total + extra_bytes || !aligned16(workspace))
     return QUAIL_ERR_INVALID_ARG;
 
   DeviceState* st = nullptr;
   const quail_status ds = device_state(&st);
   if (ds != QUAIL_OK) return ds;
-  if (d.total_suffix_tokens == 0) return QUAIL_OK;  // nothing to compute
+  *stp = st;
+  if (d.total_suffix_tokens == 0) {  // nothing to compute
+    *nothing = true;
+    return QUAIL_OK;
+  }
 
   const int D = d.head_dim;
   const int tok = 128 / group;
-  quail::CascadeMaps maps;
+  quail::CascadeMaps& maps = *mp;
   std::memset(&maps, 0, sizeof(maps));
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
@@ -251,7 +264,8 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
   }
   if (!ok) return QUAIL_ERR_CUDA;
 
-  quail::CascadeParams p;
+  quail::CascadeParams& p = *pp;
+  std::memset(&p, 0, sizeof(p));
   p.num_anchors = d.num_anchors;
   p.num_suffixes = d.num_suffixes;
   p.total_anchor_tokens = d.total_anchor_tokens;
@@ -288,14 +302,149 @@ quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_su
   p.redo_list = reinterpret_cast<int32_t*>(wsb + wl.redo_list);
   p.k_anc_bf16 = fp8 ? wsb + wl.k_anc_bf16 : nullptr;
   p.v_anc_bf16 = fp8 ? wsb + wl.v_anc_bf16 : nullptr;
+  p.mode = quail::kFused;
+  p.merge = 0;
+  p.o_part = nullptr;
+  p.lse_part = nullptr;
   p.err_word = st->err_word;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
     p.timeout_ns = g_timeout_ns;
     p.inject_skip_first_kv = g_inject_skip;
   }
-  const cudaError_t e = quail::launch_cascade(p, maps, D, fp8, st->num_sms,
+  return QUAIL_OK;
+}
+
+// Extra workspace of the two-pass variant after the cascade's own: fp32 O_a [T_S, Hq, d],
+// lse_a and lse_s [T_S, Hq].
+struct TwoPassLayout {
+  size_t o_part, lse_part, lse_s, total;
+};
+TwoPassLayout two_pass_layout(const quail_cascade_desc& d, size_t base) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t rows = static_cast<size_t>(d.total_suffix_tokens) * d.num_q_heads;
+  TwoPassLayout t;
+  t.o_part = up(base);
+  t.lse_part = up(t.o_part + rows * d.head_dim * 4);
+  t.lse_s = up(t.lse_part + rows * 4);
+  t.total = up(t.lse_s + rows * 4);
+  return t;
+}
+
+}  // namespace
+
+extern "C" {
+
+quail_status quail_cascade_attn(const quail_cascade_desc* desc, const void* q_suf,
+                                const void* k_anc, const void* v_anc, const void* k_suf,
+                                const void* v_suf, const int32_t* anchor_offsets,
+                                const int32_t* anchor_suffix_ptr,
+                                const int32_t* suffix_offsets, const float* k_scale,
+                                const float* v_scale, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes,
+                                quail_stream_t stream) {
+  quail::CascadeParams p;
+  quail::CascadeMaps maps;
+  DeviceState* st = nullptr;
+  size_t used = 0;
+  bool nothing = false;
+  const quail_status s = prepare_cascade(desc, q_suf, k_anc, v_anc, k_suf, v_suf,
+                                         anchor_offsets, anchor_suffix_ptr, suffix_offsets,
+                                         k_scale, v_scale, out, lse, workspace, workspace_bytes,
+                                         0, &p, &maps, &st, &used, &nothing);
+  if (s != QUAIL_OK || nothing) return s;
+  const cudaError_t e = quail::launch_cascade(p, maps, desc->head_dim, p.fp8, st->num_sms,
                                               reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QUAIL_OK : QUAIL_ERR_CUDA;
+}
+
+}  // extern "C"
+
+// quail_cascade_attn that also forms the max |x| of the suffix K and V per (suffix, KV
+// head) into k_amax / v_amax ([S, Hkv] fp32, zeroed here): the causal prefill's path.
+quail_status quail::cascade_attn_with_amax(const quail_cascade_desc* desc, const void* q_suf,
+                                           const void* k_anc, const void* v_anc,
+                                           const void* k_suf, const void* v_suf,
+                                           const int32_t* anchor_offsets,
+                                           const int32_t* anchor_suffix_ptr,
+                                           const int32_t* suffix_offsets, void* out, float* lse,
+                                           float* k_amax, float* v_amax, void* workspace,
+                                           size_t workspace_bytes, quail_stream_t stream) {
+  quail::CascadeParams p;
+  quail::CascadeMaps maps;
+  DeviceState* st = nullptr;
+  size_t used = 0;
+  bool nothing = false;
+  const quail_status s = prepare_cascade(desc, q_suf, k_anc, v_anc, k_suf, v_suf,
+                                         anchor_offsets, anchor_suffix_ptr, suffix_offsets,
+                                         nullptr, nullptr, out, lse, workspace, workspace_bytes,
+                                         0, &p, &maps, &st, &used, &nothing);
+  if (s != QUAIL_OK) return s;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const size_t n = static_cast<size_t>(desc->num_suffixes) * desc->num_kv_heads * sizeof(float);
+  if (n > 0 && (cudaMemsetAsync(k_amax, 0, n, cs) != cudaSuccess ||
+                cudaMemsetAsync(v_amax, 0, n, cs) != cudaSuccess))
+    return QUAIL_ERR_CUDA;
+  if (nothing) return QUAIL_OK;
+  p.k_amax = k_amax;
+  p.v_amax = v_amax;
+  const cudaError_t e = quail::launch_cascade(p, maps, desc->head_dim, false, st->num_sms, cs);
+  return e == cudaSuccess ? QUAIL_OK : QUAIL_ERR_CUDA;
+}
+
+extern "C" {
+
+size_t quail_cascade_two_pass_workspace_size(const quail_cascade_desc* desc) {
+  const size_t base = quail_cascade_workspace_size(desc);
+  if (base == 0 || desc->total_suffix_tokens < 0 ||
+      (desc->head_dim != 64 && desc->head_dim != 128))
+    return 0;
+  return two_pass_layout(*desc, base).total;
+}
+
+quail_status quail_cascade_attn_two_pass(const quail_cascade_desc* desc, const void* q_suf,
+                                         const void* k_anc, const void* v_anc,
+                                         const void* k_suf, const void* v_suf,
+                                         const int32_t* anchor_offsets,
+                                         const int32_t* anchor_suffix_ptr,
+                                         const int32_t* suffix_offsets, const float* k_scale,
+                                         const float* v_scale, int32_t merge_in_suffix_pass,
+                                         void* out, float* lse, void* workspace,
+                                         size_t workspace_bytes, quail_stream_t stream) {
+  if (desc == nullptr || (merge_in_suffix_pass != 0 && merge_in_suffix_pass != 1))
+    return QUAIL_ERR_INVALID_ARG;
+  const size_t base = quail_cascade_workspace_size(desc);
+  const size_t need = quail_cascade_two_pass_workspace_size(desc);
+  quail::CascadeParams p;
+  quail::CascadeMaps maps;
+  DeviceState* st = nullptr;
+  size_t used = 0;
+  bool nothing = false;
+  const quail_status s = prepare_cascade(
+      desc, q_suf, k_anc, v_anc, k_suf, v_suf, anchor_offsets, anchor_suffix_ptr,
+      suffix_offsets, k_scale, v_scale, out, lse, workspace, workspace_bytes,
+      need > base ? need - base : 0, &p, &maps, &st, &used, &nothing);
+  if (s != QUAIL_OK || nothing) return s;
+  const TwoPassLayout tl = two_pass_layout(*desc, used);
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  float* lse_a = reinterpret_cast<float*>(wsb + tl.lse_part);
+  float* lse_s = reinterpret_cast<float*>(wsb + tl.lse_s);
+  const int64_t rows = desc->total_suffix_tokens * desc->num_q_heads;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  p.o_part = reinterpret_cast<float*>(wsb + tl.o_part);
+  p.lse_part = lse_a;
+  // A2: anchor keys only (empty anchors get no items: their lse_a stays -inf)
+  cudaError_t e = quail::launch_fill_neg_inf(lse_a, rows, st->num_sms, cs);
+  p.mode = quail::kAnchorPass;
+  if (e == cudaSuccess) e = quail::launch_cascade(p, maps, desc->head_dim, p.fp8, st->num_sms, cs);
+  // A3: the suffix's own keys; A4 merged in its epilogue, or by the merge kernel
+  p.mode = quail::kSuffixPass;
+  p.merge = merge_in_suffix_pass;
+  if (!merge_in_suffix_pass) p.lse = lse_s;
+  if (e == cudaSuccess) e = quail::launch_cascade(p, maps, desc->head_dim, false, st->num_sms, cs);
+  if (e == cudaSuccess && !merge_in_suffix_pass)
+    e = quail::launch_lse_merge(rows, desc->head_dim, p.o_part, lse_a, lse_s, out, lse,
+                                st->num_sms, cs);
   return e == cudaSuccess ? QUAIL_OK : QUAIL_ERR_CUDA;
 }
 
@@ -362,10 +511,10 @@ quail_status quail_restricted_head(int64_t n_rows, int32_t hidden, float eps, co
   return e == cudaSuccess ? QUAIL_OK : QUAIL_ERR_CUDA;
 }
 
-quail_status quail_quantize_kv_fp8(int32_t num_anchors, const int32_t* anchor_offsets,
-                                   int64_t total_anchor_tokens, int32_t num_kv_heads,
-                                   int32_t head_dim, const void* kv_bf16, void* kv_e4m3,
-                                   float* scale, quail_stream_t stream) {
+static quail_status quantize_checks(int32_t num_anchors, const int32_t* anchor_offsets,
+                                    int64_t total_anchor_tokens, int32_t num_kv_heads,
+                                    int32_t head_dim, const void* kv_bf16, void* kv_e4m3,
+                                    float* scale) {
   if (num_anchors < 0 || total_anchor_tokens < 0 || total_anchor_tokens > (1ll << 31) - 1 ||
       num_kv_heads <= 0)
     return QUAIL_ERR_INVALID_ARG;
@@ -378,13 +527,83 @@ quail_status quail_quantize_kv_fp8(int32_t num_anchors, const int32_t* anchor_of
     return QUAIL_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(scale) | reinterpret_cast<uintptr_t>(anchor_offsets)) & 3u)
     return QUAIL_ERR_INVALID_ARG;
+  return QUAIL_OK;
+}
+
+quail_status quail_quantize_kv_fp8(int32_t num_anchors, const int32_t* anchor_offsets,
+                                   int64_t total_anchor_tokens, int32_t num_kv_heads,
+                                   int32_t head_dim, const void* kv_bf16, void* kv_e4m3,
+                                   float* scale, quail_stream_t stream) {
+  const quail_status c = quantize_checks(num_anchors, anchor_offsets, total_anchor_tokens,
+                                         num_kv_heads, head_dim, kv_bf16, kv_e4m3, scale);
+  if (c != QUAIL_OK) return c;
   DeviceState* st = nullptr;
   const quail_status ds = device_state(&st);
   if (ds != QUAIL_OK) return ds;
-  quail::QuantArgs q{num_anchors, anchor_offsets, total_anchor_tokens, num_kv_heads, head_dim,
-                     kv_bf16, kv_e4m3, scale};
+  quail::QuantArgs q{};
+  q.num_anchors = num_anchors;
+  q.anchor_offsets = anchor_offsets;
+  q.total_tokens = total_anchor_tokens;
+  q.num_kv_heads = num_kv_heads;
+  q.head_dim = head_dim;
+  q.kv = kv_bf16;
+  q.codes = kv_e4m3;
+  q.scale = scale;
+  q.err_word = st->err_word;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    q.timeout_ns = g_timeout_ns;
+  }
+  if (total_anchor_tokens > 0) {
+    // [T_A, Hkv * d] bf16, box (hg * d, 32 rows), no swizzle; rows past T_A read as zero
+    const int hg = quail::quantize_heads_per_slab(num_kv_heads, head_dim);
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(num_kv_heads) * head_dim,
+                                static_cast<cuuint64_t>(total_anchor_tokens)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(hg * head_dim), 32};
+    const cuuint32_t estr[2] = {1, 1};
+    if (g_encode(&q.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_bf16), dims,
+                 strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return QUAIL_ERR_CUDA;
+  } else {
+    // no rows: only the scales (1 each) are written
+    const cudaError_t e = quail::launch_quantize_kv_fp8_scaled(
+        q, nullptr, st->num_sms, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QUAIL_OK : QUAIL_ERR_CUDA;
+  }
   const cudaError_t e =
       quail::launch_quantize_kv_fp8(q, st->num_sms, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QUAIL_OK : QUAIL_ERR_CUDA;
+}
+
+quail_status quail_quantize_kv_fp8_with_scales(int32_t num_anchors,
+                                               const int32_t* anchor_offsets,
+                                               int64_t total_anchor_tokens,
+                                               int32_t num_kv_heads, int32_t head_dim,
+                                               const void* kv_bf16, const float* amax,
+                                               void* kv_e4m3, float* scale,
+                                               quail_stream_t stream) {
+  const quail_status c = quantize_checks(num_anchors, anchor_offsets, total_anchor_tokens,
+                                         num_kv_heads, head_dim, kv_bf16, kv_e4m3, scale);
+  if (c != QUAIL_OK) return c;
+  if (num_anchors > 0 && (amax == nullptr || (reinterpret_cast<uintptr_t>(amax) & 3u)))
+    return QUAIL_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  const quail_status ds = device_state(&st);
+  if (ds != QUAIL_OK) return ds;
+  quail::QuantArgs q{};
+  q.num_anchors = num_anchors;
+  q.anchor_offsets = anchor_offsets;
+  q.total_tokens = total_anchor_tokens;
+  q.num_kv_heads = num_kv_heads;
+  q.head_dim = head_dim;
+  q.kv = kv_bf16;
+  q.codes = kv_e4m3;
+  q.scale = scale;
+  const cudaError_t e = quail::launch_quantize_kv_fp8_scaled(
+      q, amax, st->num_sms, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QUAIL_OK : QUAIL_ERR_CUDA;
 }
 

@@ -33,7 +33,10 @@
 //   warp 10     fill checker: folds the V and next-K fills into the P-ready barrier
 //   warps 0-3   softmax of query tile 0, one thread per TMEM lane (= query row)
 //   warps 4-7   softmax of query tile 1
-//   warp 11     idle (it completes the third warpgroup for the register split)
+//   warp 11     idle (it completes the third warpgroup for the register split), or, in
+//               the causal prefill's instance with K/V amax, the amax reader: it takes
+//               max |x| of each query token's own K and V rows from the tiles in shared
+//               memory and holds each tile's slot until it has read it
 // TMEM (512 columns): tile q uses S/P at columns 256q .. +127 and O at 256q+128 .. +255.
 // The two query tiles share every anchor KV tile loaded into shared memory and ping-pong:
 // while one warpgroup exponentiates its scores the tensor core works on the other tile.
@@ -68,6 +71,7 @@ constexpr int kThreads = 384;             // three warpgroups
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 constexpr int kWarpFillCheck = 10;
+constexpr int kWarpAmax = 11;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: O is rescaled only past 2^8
 // Fast kernel bounds (P = 2^(s c) with no max subtracted); outside them the item goes to
 // the exact kernel. The row sum l = sum P must lie in [2^-64, 2^32]: every P <= l <= 2^32
@@ -191,6 +195,21 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   uint64_t r;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
+}
+
+// max |x| of 8 bf16 at a 16-byte aligned shared-memory address
+__device__ __forceinline__ float absmax_bf16x8_smem(const uint8_t* p) {
+  uint32_t w[4];
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+               : "r"(smem_u32(p)));
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m = fmaxf(m, fabsf(__uint_as_float(w[i] << 16)));
+    m = fmaxf(m, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+  }
+  return m;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -327,20 +346,30 @@ __device__ __forceinline__ void softmax_tile_exact(uint32_t t_s, uint32_t t_o, b
   tmem_wait_st();
 }
 
-// Fast kernel: P = 2^(s c) against the fixed reference m = 0 (no max pass, no rescale).
+// Fast kernel: P = 2^(s c - m_ref) against a fixed reference m_ref, the row max of the
+// item's first tile (0 when the row sees no key of that tile): one max pass per item
+// instead of one per tile, and no rescale of O afterwards. Wide logit ranges stay on the
+// fast path as long as no later tile exceeds the first one's max by ~2^32 in P.
 template <int NC, bool SCALED>
-__device__ __forceinline__ void softmax_tile_spec(uint32_t t_s, bool masked, int lo_c, int hi_c,
-                                                  float c, float pscale, float& l) {
+__device__ __forceinline__ void softmax_tile_spec(uint32_t t_s, bool first, bool masked,
+                                                  int lo_c, int hi_c, float c, float pscale,
+                                                  float& m_ref, float& l) {
   float s[NC];
   load_s<NC>(t_s, masked, lo_c, hi_c, s);
-  l += exp_store<NC, SCALED>(s, c, 0.0f, pscale, t_s + NC / 2);
+  if (first) {
+    const float m = row_max<NC>(s) * c;
+    m_ref = (m == -INFINITY) ? 0.0f : m;
+  }
+  l += exp_store<NC, SCALED>(s, c, m_ref, pscale, t_s + NC / 2);
   tmem_wait_st();
 }
 
 // ---------------------------------------------------------------------------------
 // EXACT = false: the fast kernel over all work items. EXACT = true: the exact kernel over
 // the items the fast kernel listed in redo_list (its CTAs return at once if none).
-template <int D, bool FP8, bool EXACT>
+// AMAX (fast kernel of the causal prefill only): warp 11 also forms the K/V amax of every
+// suffix token row; the K/V slots then take a second release arrival from it.
+template <int D, bool FP8, bool EXACT, bool AMAX>
 __global__ void __launch_bounds__(kThreads, 1)
 cascade_attn_kernel(const __grid_constant__ CascadeParams p,
                     const __grid_constant__ CascadeMaps maps) {
@@ -370,9 +399,9 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
     }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->k_empty[s], AMAX ? 2 : 1);
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
+      mbar_init(&bars->v_empty[s], AMAX ? 2 : 1);
     }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -499,6 +528,98 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         if (v_arm[s]) drain_wait(&bars->v_full[s], (v_arm[s] - 1) & 1u, dl);
       }
     }
+   } else if (AMAX && warp == kWarpAmax) {
+    // ------------------------------------------------ K/V amax reader (causal prefill)
+    // Every suffix token row is an own row (a query token) of exactly one query tile per
+    // KV head, and the tiles of that query tile's key window partition the window, so
+    // each K/V row is read here exactly once per KV head. For each tile: wait for its K
+    // and V fills, take max |x| over the rows that are query tokens of this item's tiles,
+    // and release the slot (the second arrival on its empty barriers). A row's 2 D bytes
+    // sit in D / 64 128-byte rows of the swizzled tile (the swizzle permutes 16-byte
+    // chunks within a row only), so 8 lanes read one row's 128 bytes per block.
+    uint32_t kv_seq = 0;
+    bool ok = true;
+    int item = blockIdx.x;
+    Item it = item < total_items ? load_item(p, item_id(item)) : Item{};
+    int cur = -1, s_lo = 0, s_hi = 0;  // cached suffix of the last row (prefix sums)
+    float km = 0.f, vm = 0.f;          // lane's running max for suffix `cur`, KV head cg
+    int cg = 0;
+    auto flush = [&]() {
+      if (cur >= 0) {
+        const int64_t i = static_cast<int64_t>(cur) * hkv + cg;
+        atomicMax(reinterpret_cast<unsigned*>(p.k_amax) + i, __float_as_uint(km));
+        atomicMax(reinterpret_cast<unsigned*>(p.v_amax) + i, __float_as_uint(vm));
+      }
+      cur = -1;
+      km = vm = 0.f;
+    };
+    for (; ok && item < total_items; item += stride) {
+      const Item nxt = item + stride < total_items ? load_item(p, item_id(item + stride)) : it;
+      const int nA = it.n_anchor_tiles();
+      const int n_tiles = it.n_tiles();
+      const bool sh = it.sfx_shared();
+      const int g = it.ag % hkv;
+      for (int pos = 0; pos < n_tiles; ++pos, ++kv_seq) {
+        const int slot = kv_seq % C::kStages;
+        const uint32_t ph = (kv_seq / C::kStages) & 1u;
+        ok = wait_parity_warp(wc, &bars->k_full[slot], ph) &&
+             wait_parity_warp(wc, &bars->v_full[slot], ph);
+        if (!ok) break;
+        if (pos >= nA) {
+          const int rel = pos - nA;
+          const uint8_t* kt = sKV + slot * 2 * C::kTileBytes;
+          const uint8_t* vt = kt + C::kTileBytes;
+          for (int qq = 0; qq < 2; ++qq) {
+            if (!sh && (rel & 1) != qq) continue;
+            const int base = sh ? it.ws0 + rel * kBN : it.ws(qq) + (rel >> 1) * kBN;
+            const int lo = max(it.t0 + qq * tok, base);
+            const int hi = min(it.tend(qq), base + kBN);
+            for (int r0 = lo; r0 < hi; r0 += 4) {
+              const int r = r0 + (lane >> 3);  // 4 rows per step, 8 lanes per row
+              float mk = 0.f, mv = 0.f;
+              if (r < hi) {
+#pragma unroll
+                for (int kb = 0; kb < C::kKB; ++kb) {
+                  const int off = kb * C::kBlockBytes + (r - base) * 128 + (lane & 7) * 16;
+                  mk = fmaxf(mk, absmax_bf16x8_smem(kt + off));
+                  mv = fmaxf(mv, absmax_bf16x8_smem(vt + off));
+                }
+              }
+#pragma unroll
+              for (int o = 1; o < 8; o <<= 1) {
+                mk = fmaxf(mk, __shfl_xor_sync(0xFFFFFFFFu, mk, o));
+                mv = fmaxf(mv, __shfl_xor_sync(0xFFFFFFFFu, mv, o));
+              }
+              if ((lane & 7) == 0 && r < hi) {
+                if (cur < 0 || r < s_lo || r >= s_hi || g != cg) {
+                  flush();
+                  // the suffix holding row r: largest s with suffix_offsets[s] <= r
+                  int a = 0, b = p.num_suffixes - 1;
+                  while (a < b) {
+                    const int m = (a + b + 1) >> 1;
+                    if (__ldg(p.suffix_offsets + m) <= r) a = m; else b = m - 1;
+                  }
+                  cur = a;
+                  cg = g;
+                  s_lo = __ldg(p.suffix_offsets + a);
+                  s_hi = __ldg(p.suffix_offsets + a + 1);
+                }
+                km = fmaxf(km, mk);
+                vm = fmaxf(vm, mv);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (elect_one()) {
+          mbar_arrive(&bars->k_empty[slot]);
+          mbar_arrive(&bars->v_empty[slot]);
+        }
+        __syncwarp();
+      }
+      it = nxt;
+    }
+    flush();
    } else if (warp == kWarpFillCheck) {
     // ------------------------------------------------ fill checker
     // For every group {PV(q,k), S(q,k+1)}: wait until the V(q,k) and K(q,k+1) fills it
@@ -685,7 +806,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       // FP8 anchor tiles: scores use c * k_scale, and P carries v_scale
       const float c_anc = FP8 ? c * __ldg(p.k_scale + it.ag) : c;
       const float v_sc = FP8 ? __ldg(p.v_scale + it.ag) : 1.0f;
-      float m_used = EXACT ? -INFINITY : 0.0f, l = 0.0f;
+      float m_used = EXACT ? -INFINITY : 0.0f, l = 0.0f;  // fast: set by the first tile
       for (int k = 0; k < n; ++k) {
         if (!(ok = wait_parity(wc, &bars->s_full[q], s_cnt & 1u))) break;
         ++s_cnt;
@@ -696,7 +817,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
             softmax_tile_exact<128, D, FP8>(t_s, t_o, k == 0, rem < kBN, 0, rem - 1, c_anc,
                                             v_sc, m_used, l);
           else
-            softmax_tile_spec<128, FP8>(t_s, rem < kBN, 0, rem - 1, c_anc, v_sc, l);
+            softmax_tile_spec<128, FP8>(t_s, k == 0, rem < kBN, 0, rem - 1, c_anc, v_sc,
+                                        m_used, l);
         } else {
           const int base = ws_q + (k - nA) * kBN;
           const int lo_c = vis_lo - base, hi_c = t - base;
@@ -712,9 +834,9 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
                                                 m_used, l);
           } else {
             if (nk_sfx == 64)
-              softmax_tile_spec<64, false>(t_s, mk, lo_c, hi_c, c, 1.0f, l);
+              softmax_tile_spec<64, false>(t_s, k == 0, mk, lo_c, hi_c, c, 1.0f, m_used, l);
             else
-              softmax_tile_spec<128, false>(t_s, mk, lo_c, hi_c, c, 1.0f, l);
+              softmax_tile_spec<128, false>(t_s, k == 0, mk, lo_c, hi_c, c, 1.0f, m_used, l);
           }
         }
         tc_fence_before();
@@ -730,12 +852,30 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         const int id = item_id(item);
         if (atomicExch(p.redo_flag + id, 1) == 0) p.redo_list[atomicAdd(p.redo_count, 1)] = id;
       }
+      __syncwarp();  // reconverge after the lane-0 branch (the TMEM loads are .aligned)
       if (!(ok = wait_parity(wc, &bars->o_done[q], it_count & 1u))) break;
       tc_fence_after();
-      const float inv_l = 1.0f / l;
-      const uint64_t il = f2(inv_l, inv_l);
       const int64_t orow = static_cast<int64_t>(t) * p.hq + g * G + (row % G);
+      // This launch's partial: lse_own (natural log) and O / l. The suffix pass of the
+      // two-pass variant may merge it with the anchor partial here (A4: LSE rescaling).
+      const float lse_own = (m_used + __log2f(l)) * 0.69314718055994531f;
+      float w_own = 1.0f / l, w_part = 0.0f, lse_out = lse_own;
+      const float* part = nullptr;
+      if (p.mode == kSuffixPass && p.merge && valid) {
+        const float lse_a = __ldg(p.lse_part + orow);
+        if (lse_a > -INFINITY) {  // -inf: the anchor is empty, nothing to merge
+          const float mx = fmaxf(lse_a, lse_own);
+          const float ea = expf(lse_a - mx), es = expf(lse_own - mx);
+          const float inv = 1.0f / (ea + es);
+          lse_out = mx + logf(ea + es);
+          w_part = ea * inv;
+          w_own = es * inv / l;
+          part = p.o_part + orow * D;
+        }
+      }
+      const uint64_t wo = f2(w_own, w_own), wp = f2(w_part, w_part);
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + orow * D;
+      float* out32 = p.mode == kAnchorPass ? p.o_part + orow * D : nullptr;
       // Two 32-column chunks of O per TMEM wait; each thread writes its row with 32-byte
       // stores (one full sector each).
 #pragma unroll
@@ -748,22 +888,47 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         if (valid) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
+            const int col0 = ch2 * 64 + h * 32;
+            if (out32 != nullptr) {  // anchor pass: fp32 normalised partial
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t v[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  float lo, hi;
+                  f2_split(f2_mul(f2(__uint_as_float(r[h][8 * j + 2 * e]),
+                                     __uint_as_float(r[h][8 * j + 2 * e + 1])), wo), lo, hi);
+                  v[2 * e] = __float_as_uint(lo);
+                  v[2 * e + 1] = __float_as_uint(hi);
+                }
+                st_global_v8(out32 + col0 + 8 * j, v);
+              }
+              continue;
+            }
             uint32_t pk[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
+              uint64_t o = f2_mul(f2(__uint_as_float(r[h][2 * j]),
+                                     __uint_as_float(r[h][2 * j + 1])), wo);
+              if (part != nullptr) {
+                const float2 a2 = *reinterpret_cast<const float2*>(part + col0 + 2 * j);
+                o = f2_fma(f2(a2.x, a2.y), wp, o);
+              }
               float lo, hi;
-              f2_split(f2_mul(f2(__uint_as_float(r[h][2 * j]), __uint_as_float(r[h][2 * j + 1])),
-                              il),
-                       lo, hi);
+              f2_split(o, lo, hi);
               pk[j] = pack_bf16(lo, hi);
             }
-            st_global_v8(out + ch2 * 64 + h * 32, pk);
-            st_global_v8(out + ch2 * 64 + h * 32 + 16, pk + 8);
+            st_global_v8(out + col0, pk);
+            st_global_v8(out + col0 + 16, pk + 8);
           }
         }
       }
-      if (valid && p.lse != nullptr)
-        p.lse[orow] = (m_used + __log2f(l)) * 0.69314718055994531f;
+      if (valid) {
+        if (p.mode == kAnchorPass)
+          p.lse_part[orow] = lse_own;
+        else if (p.lse != nullptr)
+          p.lse[orow] = lse_out;
+      }
       it = nxt;
     }
     tc_fence_before();
@@ -886,7 +1051,9 @@ __global__ void __launch_bounds__(1024) cascade_schedule_kernel(const CascadePar
     if (i < A) {
       const int a = order[i];
       const int ntok = so[asp[a + 1]] - so[asp[a]];
-      v = p.hkv * ((ntok + pair_tok - 1) / pair_tok);
+      // the anchor pass of the two-pass variant has nothing to do for an empty anchor
+      const bool none = p.mode == kAnchorPass && ao[a + 1] == ao[a];
+      v = none ? 0 : p.hkv * ((ntok + pair_tok - 1) / pair_tok);
     }
     int total;
     const int ex = block_exclusive_scan(v, warp_sums, total);
@@ -928,6 +1095,12 @@ __global__ void __launch_bounds__(256) cascade_items_kernel(const CascadeParams 
   r1.y = has1 ? p.seg[t1] : t1;
   r1.z = tend0;
   r1.w = has1 ? min(t1 + tok, s_end) : t1;
+  if (p.mode == kAnchorPass) {  // anchor keys only: empty suffix windows
+    r1.x = r1.z;
+    r1.y = r1.w;
+  } else if (p.mode == kSuffixPass) {  // suffix keys only: no anchor tiles
+    r0.y = 0;
+  }
   int4* dst = reinterpret_cast<int4*>(p.items + 8 * static_cast<int64_t>(item));
   dst[0] = r0;
   dst[1] = r1;
@@ -1000,7 +1173,81 @@ __global__ void __launch_bounds__(256) anchor_e4m3_to_bf16_kernel(const CascadeP
   }
 }
 
+// Two-pass variant, A4 as its own kernel: the LSE merge of the anchor partial (fp32 O_a,
+// lse_a) with the suffix partial (out holds O_s in bf16, lse_s) for every (token, query
+// head) row, in place: lse = log(e^lse_a + e^lse_s), out = e^(lse_a - lse) O_a +
+// e^(lse_s - lse) O_s. lse_a = -inf (an empty anchor) leaves O_s as it is. One warp per
+// row, D / 32 elements per lane (16-byte fp32 and 8-byte bf16 accesses for D = 128).
+template <int D>
+__global__ void __launch_bounds__(256) lse_merge_kernel(int64_t rows, const float* o_part,
+                                                        const float* lse_part,
+                                                        const float* lse_s,
+                                                        __nv_bfloat16* out, float* lse) {
+  constexpr int E = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       r < rows; r += warps) {
+    const float la = __ldg(lse_part + r), ls = __ldg(lse_s + r);
+    float wa = 0.0f, ws = 1.0f, lm = ls;
+    if (la > -INFINITY) {
+      const float mx = fmaxf(la, ls);
+      const float ea = expf(la - mx), es = expf(ls - mx);
+      const float inv = 1.0f / (ea + es);
+      wa = ea * inv;
+      ws = es * inv;
+      lm = mx + logf(ea + es);
+    }
+    __nv_bfloat16* o = out + r * D + lane * E;
+    const float* a = o_part + r * D + lane * E;
+    float va[E];
+    __nv_bfloat16 vs[E];
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const float2 x = *reinterpret_cast<const float2*>(a + e);
+      va[e] = x.x;
+      va[e + 1] = x.y;
+      const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162*>(o + e);
+      vs[e] = y.x;
+      vs[e + 1] = y.y;
+    }
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const float lo = wa * va[e] + ws * __bfloat162float(vs[e]);
+      const float hi = wa * va[e + 1] + ws * __bfloat162float(vs[e + 1]);
+      *reinterpret_cast<__nv_bfloat162*>(o + e) = __floats2bfloat162_rn(lo, hi);
+    }
+    if (lane == 0 && lse != nullptr) lse[r] = lm;
+  }
+}
+
+__global__ void __launch_bounds__(256) fill_neg_inf_kernel(float* x, int64_t n) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    x[i] = -INFINITY;
+}
+
 }  // namespace
+
+cudaError_t launch_fill_neg_inf(float* x, int64_t n, int num_sms, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, int64_t{num_sms} * 8));
+  fill_neg_inf_kernel<<<blocks, 256, 0, stream>>>(x, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_merge(int64_t rows, int head_dim, const float* o_part,
+                             const float* lse_part, const float* lse_s, void* out, float* lse,
+                             int num_sms, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  const int blocks = static_cast<int>(std::min<int64_t>((rows + 7) / 8, int64_t{num_sms} * 8));
+  auto* o = static_cast<__nv_bfloat16*>(out);
+  if (head_dim == 128)
+    lse_merge_kernel<128><<<blocks, 256, 0, stream>>>(rows, o_part, lse_part, lse_s, o, lse);
+  else
+    lse_merge_kernel<64><<<blocks, 256, 0, stream>>>(rows, o_part, lse_part, lse_s, o, lse);
+  return cudaGetLastError();
+}
 
 int64_t cascade_item_bound(int num_anchors, int64_t total_suffix_tokens, int hkv, int group) {
   const int64_t pair_tok = 2 * (128 / group);
@@ -1025,24 +1272,24 @@ CascadeWorkspace cascade_workspace_layout(int num_anchors, int64_t total_suffix_
   return w;
 }
 
-template <int D, bool FP8, bool EXACT>
+template <int D, bool FP8, bool EXACT, bool AMAX = false>
 static cudaError_t launch_attn_kernel(const CascadeParams& p, const CascadeMaps& maps,
                                       int num_sms, cudaStream_t stream) {
   using C = Cfg<D>;
   cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, cascade_attn_kernel<D, FP8, EXACT>);
+  cudaError_t e = cudaFuncGetAttributes(&attr, cascade_attn_kernel<D, FP8, EXACT, AMAX>);
   if (e != cudaSuccess) return e;
   // the register split must fit in what the block is launched with (else setmaxnreg.inc
   // would wait forever)
   if (static_cast<int64_t>(attr.numRegs) * kThreads <
       256 * Cfg<D>::kRegsSoftmax + 128 * Cfg<D>::kRegsOther)
     return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(cascade_attn_kernel<D, FP8, EXACT>,
+  e = cudaFuncSetAttribute(cascade_attn_kernel<D, FP8, EXACT, AMAX>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = p.item_bound < num_sms ? p.item_bound : num_sms;
   if (grid <= 0) return cudaSuccess;
-  cascade_attn_kernel<D, FP8, EXACT><<<grid, kThreads, C::kSmemBytes, stream>>>(p, maps);
+  cascade_attn_kernel<D, FP8, EXACT, AMAX><<<grid, kThreads, C::kSmemBytes, stream>>>(p, maps);
   return cudaGetLastError();
 }
 
@@ -1051,7 +1298,10 @@ static cudaError_t launch_attn_kernel(const CascadeParams& p, const CascadeMaps&
 template <int D, bool FP8>
 static cudaError_t launch_attn_d(const CascadeParams& p, const CascadeMaps& maps, int num_sms,
                                  cudaStream_t stream) {
-  cudaError_t e = launch_attn_kernel<D, FP8, false>(p, maps, num_sms, stream);
+  // the K/V amax (causal prefill) is formed by the fast kernel, which sees every item
+  cudaError_t e = (!FP8 && p.k_amax != nullptr)
+                      ? launch_attn_kernel<D, false, false, true>(p, maps, num_sms, stream)
+                      : launch_attn_kernel<D, FP8, false>(p, maps, num_sms, stream);
   if (e != cudaSuccess) return e;
   return launch_attn_kernel<D, FP8, true>(p, maps, num_sms, stream);
 }

@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "quail.h"
+
 namespace quail {
 
 // Status (a quail_status value) of the current device for the library: QUAIL_OK on a
@@ -37,8 +39,16 @@ struct QuantArgs {
   const void* kv;
   void* codes;
   float* scale;
+  CUtensorMap map;     // 2-D bf16 map over kv [T_A, Hkv * d], box (hg * d, 32 rows)
+  unsigned* err_word;
+  uint64_t timeout_ns;
 };
+// Heads per slab of the quantiser (the tensor map's box is hg * d wide).
+int quantize_heads_per_slab(int num_kv_heads, int head_dim);
 cudaError_t launch_quantize_kv_fp8(const QuantArgs& q, int num_sms, cudaStream_t stream);
+// With the amax of every (anchor, KV head) given ([A, Hkv] fp32, device).
+cudaError_t launch_quantize_kv_fp8_scaled(const QuantArgs& q, const float* amax, int num_sms,
+                                          cudaStream_t stream);
 
 struct JoinSelectArgs {
   int num_anchors;
@@ -88,6 +98,21 @@ struct CascadeParams {
   int32_t* redo_list;        // [item_bound] item indices, redo_count of them valid
   void* k_anc_bf16;          // FP8 anchor KV: [T_A, Hkv, D] bf16 copies of the codes
   void* v_anc_bf16;
+  // Which part of the cascade one launch sequence computes:
+  //   kFused       anchor and suffix keys in one online softmax (out, lse)
+  //   kAnchorPass  anchor keys only: fp32 normalised O_a -> o_part, lse_a -> lse_part
+  //                (anchors of length 0 get no work items; lse_part must hold -inf there)
+  //   kSuffixPass  the suffix's own keys only: out / lse as kFused, or with merge != 0
+  //                the LSE merge with (o_part, lse_part) done in the epilogue
+  int mode;
+  int merge;
+  float* o_part;             // [T_S, Hq, D] fp32
+  float* lse_part;           // [T_S, Hq] fp32 (natural log)
+  // Optional (causal prefill): max |x| of the suffix K and V per (suffix, KV head),
+  // [S, Hkv] fp32 (as bits for atomicMax; zeroed before the launch), formed from the
+  // K/V tiles already in shared memory.
+  float* k_amax;
+  float* v_amax;
   unsigned* err_word;
   uint64_t timeout_ns;
   int inject_skip_first_kv;
@@ -109,7 +134,26 @@ struct CascadeMaps {
   CUtensorMap q, k_anc, v_anc, k_suf, v_suf;
 };
 
+constexpr int kFused = 0, kAnchorPass = 1, kSuffixPass = 2;
+
+// quail_cascade_attn plus the max |x| of the suffix K and V per (suffix, KV head) into
+// k_amax / v_amax ([S, Hkv] fp32), formed by the fast kernel from the tiles it loads.
+quail_status cascade_attn_with_amax(const quail_cascade_desc* desc, const void* q_suf,
+                                    const void* k_anc, const void* v_anc, const void* k_suf,
+                                    const void* v_suf, const int32_t* anchor_offsets,
+                                    const int32_t* anchor_suffix_ptr,
+                                    const int32_t* suffix_offsets, void* out, float* lse,
+                                    float* k_amax, float* v_amax, void* workspace,
+                                    size_t workspace_bytes, quail_stream_t stream);
+
 cudaError_t launch_cascade(const CascadeParams& p, const CascadeMaps& maps, int head_dim,
                            bool fp8, int num_sms, cudaStream_t stream);
+
+// Two-pass helpers: lse_part[0, n) = -inf; and the LSE merge of the anchor partial
+// (o_part, lse_part) with the suffix partial (out, lse_s) in place into out (and lse).
+cudaError_t launch_fill_neg_inf(float* x, int64_t n, int num_sms, cudaStream_t stream);
+cudaError_t launch_lse_merge(int64_t rows, int head_dim, const float* o_part,
+                             const float* lse_part, const float* lse_s, void* out, float* lse,
+                             int num_sms, cudaStream_t stream);
 
 }  // namespace quail

@@ -61,7 +61,8 @@ quail_status quail_causal_prefill_attn(int32_t num_seqs, int64_t total_tokens,
                                        int32_t num_kv_heads, int32_t head_dim,
                                        float softmax_scale, const void* q, const void* k,
                                        const void* v, const int32_t* seq_offsets, void* out,
-                                       float* lse, void* workspace, size_t workspace_bytes,
+                                       float* lse, float* k_amax, float* v_amax,
+                                       void* workspace, size_t workspace_bytes,
                                        quail_stream_t stream) {
   // Host checks first (the cascade's, for this shape), so that nothing is launched when
   // the arguments are rejected.
@@ -84,6 +85,9 @@ quail_status quail_causal_prefill_attn(int32_t num_seqs, int64_t total_tokens,
        (reinterpret_cast<uintptr_t>(out) & 31u)))
     return QUAIL_ERR_INVALID_ARG;
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return QUAIL_ERR_INVALID_ARG;
+  if ((k_amax == nullptr) != (v_amax == nullptr) ||
+      ((reinterpret_cast<uintptr_t>(k_amax) | reinterpret_cast<uintptr_t>(v_amax)) & 3u))
+    return QUAIL_ERR_INVALID_ARG;
   const size_t need = quail_causal_prefill_workspace_size(num_seqs, total_tokens, max_seq_len,
                                                           num_q_heads, num_kv_heads, head_dim);
   if (need == 0 || workspace == nullptr || workspace_bytes < need ||
@@ -98,6 +102,11 @@ quail_status quail_causal_prefill_attn(int32_t num_seqs, int64_t total_tokens,
   prefill_meta_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(meta, num_seqs);
   if (cudaGetLastError() != cudaSuccess) return QUAIL_ERR_CUDA;
   // k and v double as the (empty) anchor key/value tensors: T_A = 0, nothing is read
+  if (k_amax != nullptr)
+    return quail::cascade_attn_with_amax(&d, q, k, v, k, v, meta, meta + 2, seq_offsets, out,
+                                         lse, k_amax, v_amax,
+                                         static_cast<uint8_t*>(workspace) + kMetaBytes,
+                                         workspace_bytes - kMetaBytes, stream);
   return quail_cascade_attn(&d, q, k, v, k, v, meta, meta + 2, seq_offsets, nullptr, nullptr,
                             out, lse, static_cast<uint8_t*>(workspace) + kMetaBytes,
                             workspace_bytes - kMetaBytes, stream);

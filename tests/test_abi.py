@@ -140,9 +140,9 @@ def test_causal_prefill_rejects_bad_arguments():
     v = lambda x: None if x is None else ctypes.c_void_p(x)
 
     def call(S=3, T=100, L=60, hq=8, hkv=2, d=128, scale=0.0, q=f, k=f, v_=f, so=f, out=f,
-             lse=None, ws=f, ws_bytes=1 << 20):
+             lse=None, ws=f, ws_bytes=1 << 20, ka=None, va=None):
         return q_lib().quail_causal_prefill_attn(S, T, L, hq, hkv, d, scale, v(q), v(k), v(v_),
-                                                 v(so), v(out), v(lse), v(ws),
+                                                 v(so), v(out), v(lse), v(ka), v(va), v(ws),
                                                  ctypes.c_size_t(ws_bytes), None)
 
     def q_lib():
@@ -160,6 +160,8 @@ def test_causal_prefill_rejects_bad_arguments():
     assert call(k=0x10008) == q.QUAIL_ERR_INVALID_ARG       # not 16-byte aligned
     assert call(ws=0x10080) == q.QUAIL_ERR_INVALID_ARG      # workspace not 256-byte aligned
     assert call(ws_bytes=64) == q.QUAIL_ERR_INVALID_ARG     # workspace too small
+    assert call(ka=0x10000) == q.QUAIL_ERR_INVALID_ARG      # k_amax without v_amax
+    assert call(ka=0x10000, va=0x10002) == q.QUAIL_ERR_INVALID_ARG   # misaligned
     assert q.causal_prefill_workspace_size(3, 100, 60, 8, 2, 128) > 256
     assert q.causal_prefill_workspace_size(-1, 100, 60, 8, 2, 128) == 0
 
@@ -180,3 +182,32 @@ def test_join_select_rejects_bad_arguments():
     assert call(sel=ctypes.c_void_p(0x10002)) == q.QUAIL_ERR_INVALID_ARG   # misaligned
     assert call(cnt=f, asp=None) == q.QUAIL_ERR_INVALID_ARG  # per-anchor counts need the CSR
     assert call(ws_bytes=ws_need - 4) == q.QUAIL_ERR_INVALID_ARG
+
+
+def test_two_pass_workspace_and_argument_checks():
+    d = _good_desc()
+    base = q.cascade_workspace_size(d)
+    two = q.cascade_two_pass_workspace_size(d)
+    rows = d.total_suffix_tokens * d.num_q_heads
+    assert two >= base + 4 * rows * (d.head_dim + 2) and two % 256 == 0
+    assert q.cascade_two_pass_workspace_size(_good_desc(head_dim=96)) == 0
+    f = ctypes.c_void_p(0x10000)
+    call = lambda desc, merge: q.lib.quail_cascade_attn_two_pass(
+        desc, f, f, f, f, f, f, f, f, None, None, merge, ctypes.c_void_p(0x10020), None, f,
+        ctypes.c_size_t(two), None)
+    assert call(None, 1) == q.QUAIL_ERR_INVALID_ARG
+    assert call(ctypes.byref(d), 2) == q.QUAIL_ERR_INVALID_ARG         # merge flag 0 or 1
+    assert q.lib.quail_cascade_attn_two_pass(
+        ctypes.byref(d), f, f, f, f, f, f, f, f, None, None, 1, ctypes.c_void_p(0x10020), None,
+        f, ctypes.c_size_t(base), None) == q.QUAIL_ERR_INVALID_ARG     # workspace too small
+
+
+def test_quantize_with_scales_rejects_bad_arguments():
+    f = ctypes.c_void_p(0x10000)
+    call = lambda A=2, ao=f, T=10, hkv=8, d=128, x=f, amax=f, c=f, sc=f: \
+        q.lib.quail_quantize_kv_fp8_with_scales(A, ao, T, hkv, d, x, amax, c, sc, None)
+    assert call(A=-1) == q.QUAIL_ERR_INVALID_ARG
+    assert call(d=96) == q.QUAIL_ERR_UNSUPPORTED
+    assert call(amax=None) == q.QUAIL_ERR_INVALID_ARG
+    assert call(amax=ctypes.c_void_p(0x10002)) == q.QUAIL_ERR_INVALID_ARG
+    assert call(x=ctypes.c_void_p(0x10008)) == q.QUAIL_ERR_INVALID_ARG
