@@ -1090,7 +1090,76 @@ def run_prefill(args):
                           "mma_floor_ms": round(plan["mma_floor_seconds"] * 1e3, 4),
                           "model_ms": round(plan["model_seconds"] * 1e3, 4),
                           "measured_ms": round(ms, 4)}
+    line["fused_quantise"] = prefill_quantise_pair(q, t, lay, out, lse, ws, ms, args, stream, pk,
+                                                   src)
     print(json.dumps(line))
+
+
+def prefill_quantise_pair(q, t, lay, out, lse, ws, prefill_ms, args, stream, pk, src):
+    """The anchors' prefill followed by their FP8 quantisation, two ways: (a) the prefill
+    emits the K/V amax per (sequence, KV head) from the tiles it loads, then
+    quail_quantize_kv_fp8_with_scales reads K and V once; (b) the plain prefill, then the
+    standalone quail_quantize_kv_fp8 (which finds the amax itself). Times (CUDA events,
+    median; the quantise calls with L2 flushed before each), HBM fractions of the quantise
+    calls (3 algorithmic bytes per element) and a bit-for-bit check that (a) and (b) give
+    the same codes and scales."""
+    T, hkv, d = t["k_suf"].shape
+    S = lay.num_suffixes
+    L = lay.max_suffix_len
+    k_amax = torch.empty(S, hkv, dtype=torch.float32, device=out.device)
+    v_amax = torch.empty_like(k_amax)
+    codes = {n: torch.empty(t[n].shape, dtype=torch.uint8, device=out.device)
+             for n in ("k_suf", "v_suf")}
+    scale = {n: torch.empty(S, hkv, dtype=torch.float32, device=out.device)
+             for n in ("k_suf", "v_suf")}
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=out.device)
+
+    def timed(fn, n, flush_l2):
+        evs = _events(n)
+        for a, b in evs:
+            if flush_l2:
+                flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+    pre_amax = lambda: q.causal_prefill_attn(t["q_suf"], t["k_suf"], t["v_suf"],
+                                             t["suffix_offsets"], out, L, lse=lse, workspace=ws,
+                                             k_amax=k_amax, v_amax=v_amax, stream=stream)
+    pre_amax()
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 10))
+    amax_ms = timed(pre_amax, steps, False)
+    scaled = {n: (lambda n=n: q.quantize_kv_fp8_with_scales(
+        t[n], t["suffix_offsets"], k_amax if n == "k_suf" else v_amax, codes[n], scale[n],
+        stream=stream)) for n in codes}
+    plain = {n: (lambda n=n: q.quantize_kv_fp8(t[n], t["suffix_offsets"], codes[n], scale[n],
+                                               stream=stream)) for n in codes}
+    for fn in list(scaled.values()) + list(plain.values()):
+        fn()
+    torch.cuda.synchronize()
+    ref = {n: (codes[n].clone(), scale[n].clone()) for n in codes}   # from the plain call
+    scaled_ms = {n: timed(scaled[n], steps, True) for n in codes}
+    same = all(torch.equal(codes[n], ref[n][0]) and torch.equal(scale[n], ref[n][1])
+               for n in codes)
+    plain_ms = {n: timed(plain[n], steps, True) for n in codes}
+    if q.get_device_error() != q.QUAIL_OK:
+        raise RuntimeError("device error in the prefill + quantise measurement")
+    del flush
+    algo = T * hkv * d * 3 + S * hkv * 4
+    frac = lambda ms_: round(algo / (ms_ / 1e3) / 1e9 / pk["hbm_gbs"], 4)
+    return {
+        "prefill_ms": round(prefill_ms, 4), "prefill_with_amax_ms": round(amax_ms, 4),
+        "quantise_with_scales_ms": {n: round(v, 4) for n, v in scaled_ms.items()},
+        "quantise_with_scales_hbm_frac": {n: frac(v) for n, v in scaled_ms.items()},
+        "standalone_quantise_ms": {n: round(v, 4) for n, v in plain_ms.items()},
+        "standalone_quantise_hbm_frac": {n: frac(v) for n, v in plain_ms.items()},
+        "pair_ms": {"amax_then_scaled": round(amax_ms + sum(scaled_ms.values()), 4),
+                    "plain_then_standalone": round(prefill_ms + sum(plain_ms.values()), 4)},
+        "codes_and_scales_identical": bool(same),
+        "algorithmic_bytes_per_quantise": algo, "peak_source": f"hbm_gbs of {src}"}
 
 
 def run_kvplan(args):

@@ -368,8 +368,9 @@ quail_status quail::cascade_attn_with_amax(const quail_cascade_desc* desc, const
                                            const int32_t* anchor_offsets,
                                            const int32_t* anchor_suffix_ptr,
                                            const int32_t* suffix_offsets, void* out, float* lse,
-                                           float* k_amax, float* v_amax, void* workspace,
-                                           size_t workspace_bytes, quail_stream_t stream) {
+                                           float* k_amax, float* v_amax, uint16_t* rowmax,
+                                           void* workspace, size_t workspace_bytes,
+                                           quail_stream_t stream) {
   quail::CascadeParams p;
   quail::CascadeMaps maps;
   DeviceState* st = nullptr;
@@ -381,13 +382,16 @@ quail_status quail::cascade_attn_with_amax(const quail_cascade_desc* desc, const
                                          0, &p, &maps, &st, &used, &nothing);
   if (s != QUAIL_OK) return s;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  const size_t n = static_cast<size_t>(desc->num_suffixes) * desc->num_kv_heads * sizeof(float);
-  if (n > 0 && (cudaMemsetAsync(k_amax, 0, n, cs) != cudaSuccess ||
-                cudaMemsetAsync(v_amax, 0, n, cs) != cudaSuccess))
-    return QUAIL_ERR_CUDA;
-  if (nothing) return QUAIL_OK;
+  if (nothing) {  // no tokens: every sequence is empty, its amax 0
+    const size_t n = static_cast<size_t>(desc->num_suffixes) * desc->num_kv_heads * sizeof(float);
+    if (n > 0 && (cudaMemsetAsync(k_amax, 0, n, cs) != cudaSuccess ||
+                  cudaMemsetAsync(v_amax, 0, n, cs) != cudaSuccess))
+      return QUAIL_ERR_CUDA;
+    return QUAIL_OK;
+  }
   p.k_amax = k_amax;
   p.v_amax = v_amax;
+  p.rowmax = rowmax;
   const cudaError_t e = quail::launch_cascade(p, maps, desc->head_dim, false, st->num_sms, cs);
   return e == cudaSuccess ? QUAIL_OK : QUAIL_ERR_CUDA;
 }

@@ -33,10 +33,7 @@
 //   warp 10     fill checker: folds the V and next-K fills into the P-ready barrier
 //   warps 0-3   softmax of query tile 0, one thread per TMEM lane (= query row)
 //   warps 4-7   softmax of query tile 1
-//   warp 11     idle (it completes the third warpgroup for the register split), or, in
-//               the causal prefill's instance with K/V amax, the amax reader: it takes
-//               max |x| of each query token's own K and V rows from the tiles in shared
-//               memory and holds each tile's slot until it has read it
+//   warp 11     idle (it completes the third warpgroup for the register split)
 // TMEM (512 columns): tile q uses S/P at columns 256q .. +127 and O at 256q+128 .. +255.
 // The two query tiles share every anchor KV tile loaded into shared memory and ping-pong:
 // while one warpgroup exponentiates its scores the tensor core works on the other tile.
@@ -71,7 +68,6 @@ constexpr int kThreads = 384;             // three warpgroups
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 constexpr int kWarpFillCheck = 10;
-constexpr int kWarpAmax = 11;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: O is rescaled only past 2^8
 // Fast kernel bounds (P = 2^(s c) with no max subtracted); outside them the item goes to
 // the exact kernel. The row sum l = sum P must lie in [2^-64, 2^32]: every P <= l <= 2^32
@@ -106,6 +102,9 @@ struct __align__(8) Bars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  // AMAX: the tile each K/V slot holds - its first row, the own rows of query tiles 0
+  // and 1 ([lo, hi) each), its KV head
+  int rec[4][6];
 };
 
 // One work item as written by cascade_items_kernel (two int4).
@@ -172,46 +171,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
-// Packed pairs of fp32 (one 64-bit register pair, f32x2 arithmetic).
-__device__ __forceinline__ uint64_t f2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-
-// max |x| of 8 bf16 at a 16-byte aligned shared-memory address
-__device__ __forceinline__ float absmax_bf16x8_smem(const uint8_t* p) {
-  uint32_t w[4];
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-               : "r"(smem_u32(p)));
-  float m = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    m = fmaxf(m, fabsf(__uint_as_float(w[i] << 16)));
-    m = fmaxf(m, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
-  }
-  return m;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -367,8 +326,8 @@ __device__ __forceinline__ void softmax_tile_spec(uint32_t t_s, bool first, bool
 // ---------------------------------------------------------------------------------
 // EXACT = false: the fast kernel over all work items. EXACT = true: the exact kernel over
 // the items the fast kernel listed in redo_list (its CTAs return at once if none).
-// AMAX (fast kernel of the causal prefill only): warp 11 also forms the K/V amax of every
-// suffix token row; the K/V slots then take a second release arrival from it.
+// AMAX (fast kernel of the causal prefill only): the producer also takes max |k| and
+// max |v| of every suffix token row, from each tile it is about to overwrite.
 template <int D, bool FP8, bool EXACT, bool AMAX>
 __global__ void __launch_bounds__(kThreads, 1)
 cascade_attn_kernel(const __grid_constant__ CascadeParams p,
@@ -399,9 +358,9 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
     }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], AMAX ? 2 : 1);
+      mbar_init(&bars->k_empty[s], 1);
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], AMAX ? 2 : 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -446,6 +405,67 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       uint32_t q_arm[2] = {0, 0}, k_arm[4] = {0, 0, 0, 0}, v_arm[4] = {0, 0, 0, 0};
       bool skip_pending = p.inject_skip_first_kv != 0;
       bool ok = true;
+      // AMAX: per-row max |x| of the K (kv = 0) or V (kv = 1) tile in `slot`, over the rows
+      // that are query tokens of the item that loaded it (each suffix token row is one of
+      // those exactly once per KV head). One lane per row: the row's 2 D bytes are D / 64
+      // 128-byte rows of the swizzled tile (the swizzle permutes 16-byte chunks within a
+      // row only, and a max does not care about order), read as 2 D / 16 independent
+      // 16-byte loads; rows r..r+31 fall on 8 bank groups, so each load takes the minimum
+      // 4 wavefronts.
+      auto read_own = [&](int slot, int kv) {
+        if (!AMAX) return;
+        const int* rc = bars->rec[slot];
+        const uint8_t* tile = sKV + slot * 2 * C::kTileBytes + kv * C::kTileBytes;
+        const int base = rc[0], g_rec = rc[5];
+        for (int qq = 0; qq < 2; ++qq) {
+          const int lo = rc[1 + 2 * qq], hi = rc[2 + 2 * qq];
+          for (int r0 = lo; r0 < hi; r0 += 32) {
+            const int r = r0 + lane;
+            if (r < hi) {
+              const uint8_t* row = tile + (r - base) * 128;
+              uint32_t m = 0;
+              // plain loads (not volatile asm), so that all of the row's loads are issued
+              // before the first max waits on one
+              uint4 w[C::kKB * 8];
+#pragma unroll
+              for (int kb = 0; kb < C::kKB; ++kb)
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                  w[kb * 8 + c] = *reinterpret_cast<const uint4*>(row + kb * C::kBlockBytes + c * 16);
+#pragma unroll
+              for (int i = 0; i < C::kKB * 8; ++i) {
+                m = absmax_bf16x2(m, w[i].x);
+                m = absmax_bf16x2(m, w[i].y);
+                m = absmax_bf16x2(m, w[i].z);
+                m = absmax_bf16x2(m, w[i].w);
+              }
+              p.rowmax[(static_cast<int64_t>(r) * hkv + g_rec) * 2 + kv] =
+                  static_cast<uint16_t>(max(m & 0xFFFFu, m >> 16));
+            }
+          }
+        }
+      };
+      // AMAX: slots whose K / V tile still has own rows to read (bit per slot). They are
+      // read while the producer would otherwise wait (a tile that has landed, polled
+      // without blocking, before each wait for a free slot), and at the latest just
+      // before the slot is overwritten.
+      uint32_t pend_k = 0, pend_v = 0;
+      auto landed = [&](uint64_t* bar, uint32_t parity) {
+        return __shfl_sync(0xFFFFFFFFu, mbar_try_wait(smem_u32(bar), parity) ? 1 : 0, 0) != 0;
+      };
+      auto service = [&]() {
+        if (!AMAX) return;
+        for (int s2 = 0; s2 < C::kStages; ++s2) {
+          if ((pend_k >> s2 & 1u) && landed(&bars->k_full[s2], (k_arm[s2] - 1) & 1u)) {
+            read_own(s2, 0);
+            pend_k &= ~(1u << s2);
+          }
+          if ((pend_v >> s2 & 1u) && landed(&bars->v_full[s2], (v_arm[s2] - 1) & 1u)) {
+            read_own(s2, 1);
+            pend_v &= ~(1u << s2);
+          }
+        }
+      };
       int item = blockIdx.x;
       Item it = item < total_items ? load_item(p, item_id(item)) : Item{};
       for (; ok && item < total_items; item += stride, ++it_count) {
@@ -479,7 +499,14 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           }
           uint8_t* k_dst = sKV + slot * 2 * C::kTileBytes;
           uint8_t* v_dst = k_dst + C::kTileBytes;
+          service();
           if (!(ok = wait_parity_warp(wc, &bars->k_empty[slot], ph ^ 1u))) break;
+          // the slot's previous tile is consumed and has landed: its own K rows, if not
+          // read yet, before the load below overwrites them
+          if (AMAX && (pend_k >> slot & 1u)) {
+            read_own(slot, 0);
+            pend_k &= ~(1u << slot);
+          }
           if (skip_pending) {
             skip_pending = false;  // fault injection: this tile's K never arrives
           } else {
@@ -507,7 +534,34 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
             }
             if (!ok) break;
           }
+          service();
           if (!(ok = wait_parity_warp(wc, &bars->v_empty[slot], ph ^ 1u))) break;
+          if (AMAX) {
+            if (pend_v >> slot & 1u) read_own(slot, 1);
+            // record this tile: own rows of the query tiles whose window it covers
+            bool own = false;
+            for (int qq = 0; qq < 2; ++qq) {
+              const int rel = pos - nA;
+              const bool mine = pos >= nA && (sh || (rel & 1) == qq);
+              own |= mine && min(it.tend(qq), row + kBN) > max(it.t0 + qq * tok, row);
+            }
+            __syncwarp();
+            if (lane == 0) {
+              int* rc = bars->rec[slot];
+              rc[0] = row;
+              rc[5] = g;
+              for (int qq = 0; qq < 2; ++qq) {
+                const int rel = pos - nA;
+                const bool mine = pos >= nA && (sh || (rel & 1) == qq);
+                rc[1 + 2 * qq] = mine ? max(it.t0 + qq * tok, row) : 0;
+                rc[2 + 2 * qq] = mine ? min(it.tend(qq), row + kBN) : 0;
+              }
+            }
+            __syncwarp();
+            // the K half of this slot is being loaded too (above)
+            pend_k = own ? (pend_k | (1u << slot)) : (pend_k & ~(1u << slot));
+            pend_v = own ? (pend_v | (1u << slot)) : (pend_v & ~(1u << slot));
+          }
           ++v_arm[slot];
           if (leader) {
             mbar_arrive_expect_tx(&bars->v_full[slot], C::kTileBytes);
@@ -524,102 +578,16 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       for (int q = 0; q < 2; ++q)
         if (q_arm[q]) drain_wait(&bars->q_full[q], (q_arm[q] - 1) & 1u, dl);
       for (int s = 0; s < C::kStages; ++s) {
-        if (k_arm[s]) drain_wait(&bars->k_full[s], (k_arm[s] - 1) & 1u, dl);
-        if (v_arm[s]) drain_wait(&bars->v_full[s], (v_arm[s] - 1) & 1u, dl);
+        bool landed = true;
+        if (k_arm[s]) landed &= drain_wait(&bars->k_full[s], (k_arm[s] - 1) & 1u, dl);
+        if (v_arm[s]) landed &= drain_wait(&bars->v_full[s], (v_arm[s] - 1) & 1u, dl);
+        // AMAX: the tiles still in the ring were never overwritten; read them now
+        if (AMAX && ok && landed && k_arm[s] && v_arm[s]) {
+          if (pend_k >> s & 1u) read_own(s, 0);
+          if (pend_v >> s & 1u) read_own(s, 1);
+        }
       }
     }
-   } else if (AMAX && warp == kWarpAmax) {
-    // ------------------------------------------------ K/V amax reader (causal prefill)
-    // Every suffix token row is an own row (a query token) of exactly one query tile per
-    // KV head, and the tiles of that query tile's key window partition the window, so
-    // each K/V row is read here exactly once per KV head. For each tile: wait for its K
-    // and V fills, take max |x| over the rows that are query tokens of this item's tiles,
-    // and release the slot (the second arrival on its empty barriers). A row's 2 D bytes
-    // sit in D / 64 128-byte rows of the swizzled tile (the swizzle permutes 16-byte
-    // chunks within a row only), so 8 lanes read one row's 128 bytes per block.
-    uint32_t kv_seq = 0;
-    bool ok = true;
-    int item = blockIdx.x;
-    Item it = item < total_items ? load_item(p, item_id(item)) : Item{};
-    int cur = -1, s_lo = 0, s_hi = 0;  // cached suffix of the last row (prefix sums)
-    float km = 0.f, vm = 0.f;          // lane's running max for suffix `cur`, KV head cg
-    int cg = 0;
-    auto flush = [&]() {
-      if (cur >= 0) {
-        const int64_t i = static_cast<int64_t>(cur) * hkv + cg;
-        atomicMax(reinterpret_cast<unsigned*>(p.k_amax) + i, __float_as_uint(km));
-        atomicMax(reinterpret_cast<unsigned*>(p.v_amax) + i, __float_as_uint(vm));
-      }
-      cur = -1;
-      km = vm = 0.f;
-    };
-    for (; ok && item < total_items; item += stride) {
-      const Item nxt = item + stride < total_items ? load_item(p, item_id(item + stride)) : it;
-      const int nA = it.n_anchor_tiles();
-      const int n_tiles = it.n_tiles();
-      const bool sh = it.sfx_shared();
-      const int g = it.ag % hkv;
-      for (int pos = 0; pos < n_tiles; ++pos, ++kv_seq) {
-        const int slot = kv_seq % C::kStages;
-        const uint32_t ph = (kv_seq / C::kStages) & 1u;
-        ok = wait_parity_warp(wc, &bars->k_full[slot], ph) &&
-             wait_parity_warp(wc, &bars->v_full[slot], ph);
-        if (!ok) break;
-        if (pos >= nA) {
-          const int rel = pos - nA;
-          const uint8_t* kt = sKV + slot * 2 * C::kTileBytes;
-          const uint8_t* vt = kt + C::kTileBytes;
-          for (int qq = 0; qq < 2; ++qq) {
-            if (!sh && (rel & 1) != qq) continue;
-            const int base = sh ? it.ws0 + rel * kBN : it.ws(qq) + (rel >> 1) * kBN;
-            const int lo = max(it.t0 + qq * tok, base);
-            const int hi = min(it.tend(qq), base + kBN);
-            for (int r0 = lo; r0 < hi; r0 += 4) {
-              const int r = r0 + (lane >> 3);  // 4 rows per step, 8 lanes per row
-              float mk = 0.f, mv = 0.f;
-              if (r < hi) {
-#pragma unroll
-                for (int kb = 0; kb < C::kKB; ++kb) {
-                  const int off = kb * C::kBlockBytes + (r - base) * 128 + (lane & 7) * 16;
-                  mk = fmaxf(mk, absmax_bf16x8_smem(kt + off));
-                  mv = fmaxf(mv, absmax_bf16x8_smem(vt + off));
-                }
-              }
-#pragma unroll
-              for (int o = 1; o < 8; o <<= 1) {
-                mk = fmaxf(mk, __shfl_xor_sync(0xFFFFFFFFu, mk, o));
-                mv = fmaxf(mv, __shfl_xor_sync(0xFFFFFFFFu, mv, o));
-              }
-              if ((lane & 7) == 0 && r < hi) {
-                if (cur < 0 || r < s_lo || r >= s_hi || g != cg) {
-                  flush();
-                  // the suffix holding row r: largest s with suffix_offsets[s] <= r
-                  int a = 0, b = p.num_suffixes - 1;
-                  while (a < b) {
-                    const int m = (a + b + 1) >> 1;
-                    if (__ldg(p.suffix_offsets + m) <= r) a = m; else b = m - 1;
-                  }
-                  cur = a;
-                  cg = g;
-                  s_lo = __ldg(p.suffix_offsets + a);
-                  s_hi = __ldg(p.suffix_offsets + a + 1);
-                }
-                km = fmaxf(km, mk);
-                vm = fmaxf(vm, mv);
-              }
-            }
-          }
-        }
-        __syncwarp();
-        if (elect_one()) {
-          mbar_arrive(&bars->k_empty[slot]);
-          mbar_arrive(&bars->v_empty[slot]);
-        }
-        __syncwarp();
-      }
-      it = nxt;
-    }
-    flush();
    } else if (warp == kWarpFillCheck) {
     // ------------------------------------------------ fill checker
     // For every group {PV(q,k), S(q,k+1)}: wait until the V(q,k) and K(q,k+1) fills it
@@ -950,13 +918,16 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
 __global__ void __launch_bounds__(256) cascade_segments_kernel(const CascadeParams p) {
   const int S = p.num_suffixes;
   const int64_t T = p.total_suffix_tokens;
-  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < S; s += gridDim.x * blockDim.x) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  // one warp per suffix: its lanes write the suffix's tokens
+  for (int s = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; s < S; s += warps) {
     const int lo = __ldg(p.suffix_offsets + s), hi = __ldg(p.suffix_offsets + s + 1);
     if (lo < 0 || hi < lo || hi > T || hi - lo > p.max_suffix_len) {
-      atomicOr(p.flag, 1);
+      if (lane == 0) atomicOr(p.flag, 1);
       continue;
     }
-    for (int t = lo; t < hi; ++t) p.seg[t] = lo;
+    for (int t = lo + lane; t < hi; t += 32) p.seg[t] = lo;
   }
 }
 
@@ -1173,6 +1144,39 @@ __global__ void __launch_bounds__(256) anchor_e4m3_to_bf16_kernel(const CascadeP
   }
 }
 
+// Causal prefill with K/V amax: per (suffix, KV head), the max of the per-row maxima the
+// producer stored (bf16 bit patterns of non-negative values order like integers). One
+// block per suffix; suffixes whose offsets fail the checks are skipped.
+__global__ void __launch_bounds__(256) kv_amax_reduce_kernel(const CascadeParams p) {
+  // one warp per (suffix, KV head); lanes stride over the suffix's rows
+  const int hkv = p.hkv;
+  const int lane = threadIdx.x & 31;
+  const int64_t pairs = static_cast<int64_t>(p.num_suffixes) * hkv;
+  const int64_t warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       w < pairs; w += warps) {
+    const int s = static_cast<int>(w / hkv), g = static_cast<int>(w % hkv);
+    const int lo = __ldg(p.suffix_offsets + s), hi = __ldg(p.suffix_offsets + s + 1);
+    uint32_t m = 0;  // packed (max |k|, max |v|) bf16 patterns
+    if (lo >= 0 && hi >= lo && hi <= p.total_suffix_tokens) {
+      const uint32_t* rm = reinterpret_cast<const uint32_t*>(p.rowmax);
+      for (int r = lo + lane; r < hi; r += 32) {
+        uint32_t v = __ldg(rm + static_cast<int64_t>(r) * hkv + g);
+        asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(v));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const uint32_t v = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+      asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(v));
+    }
+    if (lane == 0) {
+      p.k_amax[w] = __uint_as_float((m & 0xFFFFu) << 16);
+      p.v_amax[w] = __uint_as_float(m & 0xFFFF0000u);
+    }
+  }
+}
+
 // Two-pass variant, A4 as its own kernel: the LSE merge of the anchor partial (fp32 O_a,
 // lse_a) with the suffix partial (out holds O_s in bf16, lse_s) for every (token, query
 // head) row, in place: lse = log(e^lse_a + e^lse_s), out = e^(lse_a - lse) O_a +
@@ -1299,11 +1303,16 @@ template <int D, bool FP8>
 static cudaError_t launch_attn_d(const CascadeParams& p, const CascadeMaps& maps, int num_sms,
                                  cudaStream_t stream) {
   // the K/V amax (causal prefill) is formed by the fast kernel, which sees every item
-  cudaError_t e = (!FP8 && p.k_amax != nullptr)
-                      ? launch_attn_kernel<D, false, false, true>(p, maps, num_sms, stream)
-                      : launch_attn_kernel<D, FP8, false>(p, maps, num_sms, stream);
+  const bool amax = !FP8 && p.k_amax != nullptr;
+  cudaError_t e = amax ? launch_attn_kernel<D, false, false, true>(p, maps, num_sms, stream)
+                       : launch_attn_kernel<D, FP8, false>(p, maps, num_sms, stream);
   if (e != cudaSuccess) return e;
-  return launch_attn_kernel<D, FP8, true>(p, maps, num_sms, stream);
+  e = launch_attn_kernel<D, FP8, true>(p, maps, num_sms, stream);
+  if (e != cudaSuccess || !amax || p.num_suffixes == 0) return e;
+  const int64_t pairs = static_cast<int64_t>(p.num_suffixes) * p.hkv;
+  const int blocks = static_cast<int>(std::min<int64_t>((pairs + 7) / 8, int64_t{num_sms} * 8));
+  kv_amax_reduce_kernel<<<blocks, 256, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_cascade(const CascadeParams& p, const CascadeMaps& maps, int head_dim,
@@ -1312,7 +1321,7 @@ cudaError_t launch_cascade(const CascadeParams& p, const CascadeMaps& maps, int 
   if (e != cudaSuccess) return e;
   if (p.num_suffixes > 0) {
     const int blocks = static_cast<int>(
-        std::min<int64_t>((p.num_suffixes + 255) / 256, static_cast<int64_t>(num_sms) * 8));
+        std::min<int64_t>((p.num_suffixes + 7) / 8, static_cast<int64_t>(num_sms) * 8));
     cascade_segments_kernel<<<blocks, 256, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

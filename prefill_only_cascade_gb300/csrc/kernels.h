@@ -109,10 +109,11 @@ struct CascadeParams {
   float* o_part;             // [T_S, Hq, D] fp32
   float* lse_part;           // [T_S, Hq] fp32 (natural log)
   // Optional (causal prefill): max |x| of the suffix K and V per (suffix, KV head),
-  // [S, Hkv] fp32 (as bits for atomicMax; zeroed before the launch), formed from the
-  // K/V tiles already in shared memory.
+  // [S, Hkv] fp32, formed from the K/V tiles already in shared memory via per-row
+  // maxima rowmax [T_S, Hkv, 2] (bf16 bit patterns of max |k|, max |v|).
   float* k_amax;
   float* v_amax;
+  uint16_t* rowmax;
   unsigned* err_word;
   uint64_t timeout_ns;
   int inject_skip_first_kv;
@@ -138,13 +139,15 @@ constexpr int kFused = 0, kAnchorPass = 1, kSuffixPass = 2;
 
 // quail_cascade_attn plus the max |x| of the suffix K and V per (suffix, KV head) into
 // k_amax / v_amax ([S, Hkv] fp32), formed by the fast kernel from the tiles it loads.
+// rowmax: [T_S, Hkv, 2] uint16 scratch for the per-row maxima.
 quail_status cascade_attn_with_amax(const quail_cascade_desc* desc, const void* q_suf,
                                     const void* k_anc, const void* v_anc, const void* k_suf,
                                     const void* v_suf, const int32_t* anchor_offsets,
                                     const int32_t* anchor_suffix_ptr,
                                     const int32_t* suffix_offsets, void* out, float* lse,
-                                    float* k_amax, float* v_amax, void* workspace,
-                                    size_t workspace_bytes, quail_stream_t stream);
+                                    float* k_amax, float* v_amax, uint16_t* rowmax,
+                                    void* workspace, size_t workspace_bytes,
+                                    quail_stream_t stream);
 
 cudaError_t launch_cascade(const CascadeParams& p, const CascadeMaps& maps, int head_dim,
                            bool fp8, int num_sms, cudaStream_t stream);

@@ -17,6 +17,12 @@ namespace {
 
 constexpr size_t kMetaBytes = 256;  // [0, 0] anchor offsets, [0, S] anchor->suffix map
 
+// Workspace: meta, then the per-row K/V maxima [T, Hkv, 2] uint16 (used when the K/V
+// amax is formed), then the cascade's own workspace.
+size_t rowmax_bytes(int64_t total_tokens, int32_t num_kv_heads) {
+  return (static_cast<size_t>(total_tokens) * num_kv_heads * 4 + 255) / 256 * 256;
+}
+
 __global__ void prefill_meta_kernel(int32_t* meta, int32_t num_seqs) {
   meta[0] = 0;  // anchor_offsets: one anchor of length 0
   meta[1] = 0;
@@ -53,7 +59,7 @@ size_t quail_causal_prefill_workspace_size(int32_t num_seqs, int64_t total_token
   const quail_cascade_desc d = prefill_desc(num_seqs, total_tokens, max_seq_len, num_q_heads,
                                             num_kv_heads, head_dim, 0.0f);
   const size_t inner = quail_cascade_workspace_size(&d);
-  return inner == 0 ? 0 : kMetaBytes + inner;
+  return inner == 0 ? 0 : kMetaBytes + rowmax_bytes(total_tokens, num_kv_heads) + inner;
 }
 
 quail_status quail_causal_prefill_attn(int32_t num_seqs, int64_t total_tokens,
@@ -102,14 +108,15 @@ quail_status quail_causal_prefill_attn(int32_t num_seqs, int64_t total_tokens,
   prefill_meta_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(meta, num_seqs);
   if (cudaGetLastError() != cudaSuccess) return QUAIL_ERR_CUDA;
   // k and v double as the (empty) anchor key/value tensors: T_A = 0, nothing is read
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  const size_t front = kMetaBytes + rowmax_bytes(total_tokens, num_kv_heads);
   if (k_amax != nullptr)
     return quail::cascade_attn_with_amax(&d, q, k, v, k, v, meta, meta + 2, seq_offsets, out,
                                          lse, k_amax, v_amax,
-                                         static_cast<uint8_t*>(workspace) + kMetaBytes,
-                                         workspace_bytes - kMetaBytes, stream);
+                                         reinterpret_cast<uint16_t*>(wsb + kMetaBytes),
+                                         wsb + front, workspace_bytes - front, stream);
   return quail_cascade_attn(&d, q, k, v, k, v, meta, meta + 2, seq_offsets, nullptr, nullptr,
-                            out, lse, static_cast<uint8_t*>(workspace) + kMetaBytes,
-                            workspace_bytes - kMetaBytes, stream);
+                            out, lse, wsb + front, workspace_bytes - front, stream);
 }
 
 }  // extern "C"

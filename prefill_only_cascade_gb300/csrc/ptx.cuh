@@ -99,6 +99,47 @@ __device__ __forceinline__ bool wait_parity_warp(const WaitCtl& w, uint64_t* bar
   return __all_sync(0xFFFFFFFFu, wait_parity(w, bar, parity));
 }
 
+// ------------------------------------------------------------------ packed fp32 pairs
+// One 64-bit register pair holding two fp32 values; f32x2 arithmetic rounds each lane
+// exactly as the scalar instruction does.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// Running max of |x| over packed bf16 pairs: |x| of a bf16 is its bit pattern with the
+// sign cleared, and non-negative bf16 values order like their 16-bit patterns, so the
+// max is one AND and one max.u16x2 per word (a NaN, whose pattern is above +inf, wins).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint32_t w) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(acc), "r"(w & 0x7FFF7FFFu));
+  return r;
+}
+// The larger of the two 16-bit halves, as the fp32 value of that bf16.
+__device__ __forceinline__ float absmax_bf16x2_value(uint32_t acc) {
+  const uint32_t m = max(acc & 0xFFFFu, acc >> 16);
+  return __uint_as_float(m << 16);
+}
+
 // ------------------------------------------------------------------ thread-block clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
