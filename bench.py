@@ -966,7 +966,10 @@ def measure_bandwidth_kernel(q, args, kind, steps):
            "steps": steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
            "config": config,
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
-                        "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
+                        "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                        "traffic": (traffic_from_profile("quantize.cu", "quantize_fp8_long.md")
+                                    if kind == "quantize" else
+                                    traffic_from_profile("head.cu", "restricted_head.md")),
                         "peak_source": f"hbm_gbs of {src}", "kernel": kernel,
                         "kernel_ms": round(ms, 4), "algorithmic_bytes_per_launch": algo_bytes},
            "cpu_baseline": cpu, "parity": parity, "gpu_launches": steps,
