@@ -393,6 +393,25 @@ void quail_set_wait_timeout_ns(uint64_t ns);
  */
 void quail_debug_inject(int32_t skip_first_kv_load);
 
+/*
+ * Kernel choice for head_dim 128 cascade calls (fused, without K/V amax). The CTA-pair
+ * kernel runs four 128-row query tiles of one (anchor, KV head) on a pair of SMs: each
+ * S = Q K^T and O += P V is one 256-row tcgen05 MMA over the pair, each SM holding its
+ * own query rows and half of every K/V tile (half the tile loads per SM). The single-SM
+ * kernel runs two query tiles on one SM, and loads a suffix window of at most 64 keys as
+ * one 64-key tile where the pair always uses 128-key tiles.
+ *   QUAIL_CTA_PAIRS_OFF     always the single-SM kernel
+ *   QUAIL_CTA_PAIRS_AUTO    (default) the pair kernel unless every query tile's suffix
+ *                           window fits in 64 keys: 128 / G + max_suffix_len - 1 <= 64
+ *   QUAIL_CTA_PAIRS_ALWAYS  always the pair kernel
+ * Both give the same results within rounding. Process-wide; set it between calls, not
+ * while another thread is launching. Returns QUAIL_ERR_INVALID_ARG for another `mode`.
+ */
+#define QUAIL_CTA_PAIRS_OFF 0
+#define QUAIL_CTA_PAIRS_AUTO 1
+#define QUAIL_CTA_PAIRS_ALWAYS 2
+quail_status quail_set_cta_pairs(int32_t mode);
+
 /* Library version, e.g. "quail-gb300 0.1". */
 const char* quail_version(void);
 

@@ -30,7 +30,7 @@ QUAIL_FP8_E4M3 = 1
 EXPORTED_SYMBOLS = (
     "quail_cascade_attn", "quail_cascade_workspace_size", "quail_restricted_head",
     "quail_quantize_kv_fp8", "quail_status_string", "quail_get_device_error",
-    "quail_set_wait_timeout_ns", "quail_debug_inject", "quail_version",
+    "quail_set_wait_timeout_ns", "quail_debug_inject", "quail_set_cta_pairs", "quail_version",
     "quail_cascade_attn_noalloc", "quail_causal_prefill_attn",
     "quail_causal_prefill_workspace_size", "quail_kv_plan", "quail_shard_anchors",
     "quail_join_select", "quail_join_select_workspace_size", "quail_shard_batch",
@@ -116,6 +116,8 @@ def _load():
     lib.quail_set_wait_timeout_ns.restype = None
     lib.quail_debug_inject.argtypes = [ctypes.c_int32]
     lib.quail_debug_inject.restype = None
+    lib.quail_set_cta_pairs.argtypes = [ctypes.c_int32]
+    lib.quail_set_cta_pairs.restype = ctypes.c_int
     lib.quail_version.argtypes = []
     lib.quail_version.restype = ctypes.c_char_p
     i32, i64 = ctypes.c_int32, ctypes.c_int64
@@ -365,6 +367,16 @@ def set_wait_timeout_ns(ns: int):
 
 def debug_inject(skip_first_kv_load: bool):
     lib.quail_debug_inject(1 if skip_first_kv_load else 0)
+
+
+CTA_PAIRS_OFF, CTA_PAIRS_AUTO, CTA_PAIRS_ALWAYS = 0, 1, 2
+
+
+def set_cta_pairs(mode: int) -> int:
+    """head_dim 128 kernel choice: CTA_PAIRS_OFF (single-SM kernel), CTA_PAIRS_AUTO (the
+    default: SM pairs unless every query tile's suffix window fits in 64 keys) or
+    CTA_PAIRS_ALWAYS. Returns the status."""
+    return lib.quail_set_cta_pairs(int(mode))
 
 
 def default_scale(head_dim: int) -> float:

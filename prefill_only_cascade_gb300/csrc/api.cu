@@ -126,6 +126,13 @@ void quail_set_wait_timeout_ns(uint64_t ns) {
   g_timeout_ns = ns == 0 ? kDefaultTimeoutNs : ns;
 }
 
+quail_status quail_set_cta_pairs(int32_t mode) {
+  if (mode != QUAIL_CTA_PAIRS_OFF && mode != QUAIL_CTA_PAIRS_AUTO && mode != QUAIL_CTA_PAIRS_ALWAYS)
+    return QUAIL_ERR_INVALID_ARG;
+  quail::set_cta_pairs(mode);
+  return QUAIL_OK;
+}
+
 void quail_debug_inject(int32_t skip_first_kv_load) {
   std::lock_guard<std::mutex> lock(g_mutex);
   g_inject_skip = skip_first_kv_load != 0;
@@ -254,13 +261,18 @@ quail_status prepare_cascade(const quail_cascade_desc* desc, const void* q_suf, 
       encode_3d(&maps.q, q_suf, d.total_suffix_tokens, d.num_q_heads, D, group, tok, bf, 2, 64) &&
       encode_3d(&maps.k_suf, k_suf, d.total_suffix_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64) &&
       encode_3d(&maps.v_suf, v_suf, d.total_suffix_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64);
+  // K with 64-row boxes: the halves of a key tile that the two CTAs of a pair load
+  ok = ok && encode_3d(&maps.k_suf64, k_suf, d.total_suffix_tokens, d.num_kv_heads, D, 1, 64,
+                       bf, 2, 64);
   if (d.total_anchor_tokens > 0) {
     ok = ok &&
          encode_3d(&maps.k_anc, k_anc_tiles, d.total_anchor_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64) &&
-         encode_3d(&maps.v_anc, v_anc_tiles, d.total_anchor_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64);
+         encode_3d(&maps.v_anc, v_anc_tiles, d.total_anchor_tokens, d.num_kv_heads, D, 1, 128, bf, 2, 64) &&
+         encode_3d(&maps.k_anc64, k_anc_tiles, d.total_anchor_tokens, d.num_kv_heads, D, 1, 64, bf, 2, 64);
   } else {
     maps.k_anc = maps.k_suf;  // never read: every anchor is empty
     maps.v_anc = maps.v_suf;
+    maps.k_anc64 = maps.k_suf64;
   }
   if (!ok) return QUAIL_ERR_CUDA;
 
@@ -304,6 +316,7 @@ quail_status prepare_cascade(const quail_cascade_desc* desc, const void* q_suf, 
   p.v_anc_bf16 = fp8 ? wsb + wl.v_anc_bf16 : nullptr;
   p.mode = quail::kFused;
   p.merge = 0;
+  p.tiles_per_item = 2;  // launch_cascade picks the item shape for the kernel it runs
   p.o_part = nullptr;
   p.lse_part = nullptr;
   p.err_word = st->err_word;

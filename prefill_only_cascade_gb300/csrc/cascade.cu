@@ -45,6 +45,7 @@
 // their P (P = p * v_scale, while the row sum keeps p), so O accumulates true values.
 // Converting once per call instead of once per work item keeps the tensor core fed: a
 // (anchor, KV head) is read by hundreds of work items.
+#include <atomic>
 #include <algorithm>
 
 #include <cuda_bf16.h>
@@ -102,10 +103,12 @@ struct __align__(8) Bars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  uint32_t peer_abort;  // CTA pairs: the other CTA of the pair gave up on a wait
   // AMAX: the tile each K/V slot holds - its first row, the own rows of query tiles 0
   // and 1 ([lo, hi) each), its KV head
   int rec[4][6];
 };
+static_assert(sizeof(Bars) <= 1024, "barriers fit in the last kilobyte of shared memory");
 
 // One work item as written by cascade_items_kernel (two int4).
 struct Item {
@@ -139,6 +142,24 @@ __device__ __forceinline__ int4 ld_nc_v4(const int32_t* p) {
 }
 
 __device__ __forceinline__ Item load_item(const CascadeParams& p, int item) {
+  if (p.tiles_per_item == 4) {
+    // half h of quad item / 2 (the exact kernel after the CTA-pair kernel): its query
+    // tiles 2h and 2h + 1, each with its own key window
+    const int quad = item >> 1, h = item & 1;
+    const int4 a = ld_nc_v4(p.items + 12 * static_cast<int64_t>(quad));
+    const int4 b = ld_nc_v4(p.items + 12 * static_cast<int64_t>(quad) + 4);
+    const int4 c = ld_nc_v4(p.items + 12 * static_cast<int64_t>(quad) + 8);
+    const int tok = p.tok_per_tile;
+    Item it;
+    it.a_tok0 = a.x; it.la = a.y; it.ag = a.w;
+    it.t0 = a.z + 2 * h * tok;
+    it.tend0 = h ? c.x : b.z;
+    it.tend1 = h ? c.y : b.w;
+    const int t1 = it.t0 + tok;
+    it.ws0 = it.t0 < it.tend0 ? __ldg(p.seg + it.t0) : it.t0;
+    it.ws1 = t1 < it.tend1 ? __ldg(p.seg + t1) : t1;
+    return it;
+  }
   const int4 a = ld_nc_v4(p.items + 8 * static_cast<int64_t>(item));
   const int4 b = ld_nc_v4(p.items + 8 * static_cast<int64_t>(item) + 4);
   Item it;
@@ -454,15 +475,16 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         return __shfl_sync(0xFFFFFFFFu, mbar_try_wait(smem_u32(bar), parity) ? 1 : 0, 0) != 0;
       };
       auto service = [&]() {
-        if (!AMAX) return;
-        for (int s2 = 0; s2 < C::kStages; ++s2) {
-          if ((pend_k >> s2 & 1u) && landed(&bars->k_full[s2], (k_arm[s2] - 1) & 1u)) {
-            read_own(s2, 0);
-            pend_k &= ~(1u << s2);
-          }
-          if ((pend_v >> s2 & 1u) && landed(&bars->v_full[s2], (v_arm[s2] - 1) & 1u)) {
-            read_own(s2, 1);
-            pend_v &= ~(1u << s2);
+        if constexpr (AMAX) {
+          for (int s2 = 0; s2 < C::kStages; ++s2) {
+            if ((pend_k >> s2 & 1u) && landed(&bars->k_full[s2], (k_arm[s2] - 1) & 1u)) {
+              read_own(s2, 0);
+              pend_k &= ~(1u << s2);
+            }
+            if ((pend_v >> s2 & 1u) && landed(&bars->v_full[s2], (v_arm[s2] - 1) & 1u)) {
+              read_own(s2, 1);
+              pend_v &= ~(1u << s2);
+            }
           }
         }
       };
@@ -910,6 +932,468 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
   }
 }
 
+// =================================================================================
+// The fast kernel on CTA pairs (d = 128): tcgen05.mma.cta_group::2, M = 256.
+//
+// A cluster of two CTAs takes a "quad" work item: (anchor, KV head, four 128-row query
+// tiles over 4 x 128 / G consecutive suffix tokens). Query tile j of the quad is held by
+// CTA j % 2 as its pair tile q = j / 2: pair tile q is one M = 256 MMA over query tiles 2q
+// (rank 0) and 2q + 1 (rank 1), and each CTA still ping-pongs two pair tiles between its
+// softmax warpgroups. Every K/V tile (128 keys) serves all four query tiles; each CTA
+// loads and holds half of it: keys 64 r .. 64 r + 63 of the K tile (the N half of the B
+// operand of S = Q K^T) and d columns 64 r .. 64 r + 63 of the V tile (the N half of the B
+// operand of O += P V). Per SM and K16 step, S then reads 4 KB (its own query rows) + 2 KB
+// (its K half) of shared memory instead of 8 KB, and a quad has half the item boundaries
+// per query tile of a pair item.
+// Synchronisation: rank 0's MMA warp issues every MMA for both CTAs, and its commits
+// arrive on the barrier of the same name in both CTAs (slot free, S ready, query tile
+// free, O done). Both CTAs' TMA loads complete on rank 0's full barriers, for which rank 0
+// expects both halves' bytes; both CTAs' softmax warps arrive on rank 0's P-ready barrier
+// (9 arrivals: 2 x 4 softmax warps + rank 0's fill checker). Rank 1's MMA warp takes part
+// only in the TMEM allocation. Suffix tiles always use N = 128 (a 64-key tile would split
+// 32 / 32 between the CTAs, not as the 64-row K halves are loaded).
+struct PairCfg {
+  static constexpr int kKB = 2;                          // 128-byte column blocks (d = 128)
+  static constexpr int kBlockBytes = 128 * 128;          // 128 rows x 128 bytes
+  static constexpr int kQTileBytes = 2 * kBlockBytes;    // one 128-row query tile
+  static constexpr int kKHalfBlock = 64 * 128;           // 64 key rows x 128 bytes
+  static constexpr int kKHalfBytes = 2 * kKHalfBlock;    // 64 keys x d
+  static constexpr int kVHalfBytes = kBlockBytes;        // 128 keys x 64 d columns
+  static constexpr int kStageBytes = kKHalfBytes + kVHalfBytes;
+  static constexpr int kStages = 4;
+  static constexpr int kSmemQ = 2 * kQTileBytes;
+  static constexpr int kSmemKV = kStages * kStageBytes;
+  static constexpr int kSmemBytes = kSmemQ + kSmemKV + 1024 + 1024;
+};
+
+struct Quad {
+  int a_tok0, la, t0, ag;
+  int wsp[2];   // key window start of pair tile 0 / 1 (start of the suffix of its first token)
+  int tend[4];  // one past the last token of query tile j (its start when empty)
+  __device__ __forceinline__ int n_anchor_tiles() const { return (la + kBN - 1) / kBN; }
+  __device__ __forceinline__ int window(int q) const {
+    return max(max(tend[2 * q], tend[2 * q + 1]) - wsp[q], 0);
+  }
+  __device__ __forceinline__ int n_sfx_tiles() const {
+    return (max(window(0), window(1)) + kBN - 1) / kBN;
+  }
+  __device__ __forceinline__ bool sfx_shared() const { return wsp[0] == wsp[1]; }
+  __device__ __forceinline__ int n_tiles() const {
+    return n_anchor_tiles() + (sfx_shared() ? 1 : 2) * n_sfx_tiles();
+  }
+};
+__device__ __forceinline__ Quad load_quad(const CascadeParams& p, int item) {
+  const int4 a = ld_nc_v4(p.items + 12 * static_cast<int64_t>(item));
+  const int4 b = ld_nc_v4(p.items + 12 * static_cast<int64_t>(item) + 4);
+  const int4 c = ld_nc_v4(p.items + 12 * static_cast<int64_t>(item) + 8);
+  Quad it;
+  it.a_tok0 = a.x; it.la = a.y; it.t0 = a.z; it.ag = a.w;
+  it.wsp[0] = b.x; it.wsp[1] = b.y; it.tend[0] = b.z; it.tend[1] = b.w;
+  it.tend[2] = c.x; it.tend[3] = c.y;
+  return it;
+}
+
+template <bool FP8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+cascade_pair_kernel(const __grid_constant__ CascadeParams p,
+                    const __grid_constant__ CascadeMaps maps) {
+  using C = PairCfg;
+  constexpr int D = 128;
+  const int total_items = __ldg(p.prefix + p.num_anchors);  // quads
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + C::kSmemQ;
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::kSmemQ + C::kSmemKV);
+  const uint32_t rank = cluster_ctarank();
+  const bool lead = rank == 0;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&bars->q_full[q], 1);
+      mbar_init(&bars->q_empty[q], 1);
+      mbar_init(&bars->s_full[q], 1);
+      mbar_init(&bars->p_full[q], 9);  // 2 x 4 softmax warps + the fill checker
+      mbar_init(&bars->o_done[q], 1);
+    }
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    bars->peer_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc_pair(&bars->tmem_base, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrival or transfer
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  WaitCtl wc;
+  wc.timeout_ns = p.timeout_ns;
+  wc.abort_flag = &bars->abort_flag;
+  wc.err_word = p.err_word;
+
+  const int tok = p.tok_per_tile;
+  const int G = p.group;
+  const int hkv = p.hkv;
+  const int stride = gridDim.x / 2;  // clusters
+  const int first = blockIdx.x / 2;
+  // rank 0's copy of a barrier, as a shared::cluster address
+  auto lead_bar = [&](uint64_t* b) { return cluster_map(b, 0); };
+
+  if (warp >= 8) {
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg<D>::kRegsOther));
+   if (warp == kWarpProducer) {
+    // both CTAs: their query tiles and their halves of every K/V tile
+    const bool elect = elect_one();
+    if (elect) {
+      tma_prefetch_desc(&maps.q);
+      tma_prefetch_desc(&maps.k_anc64);
+      tma_prefetch_desc(&maps.v_anc);
+      tma_prefetch_desc(&maps.k_suf64);
+      tma_prefetch_desc(&maps.v_suf);
+    }
+    const uint64_t keep = l2_policy_evict_last(), stream_pol = l2_policy_evict_first();
+    uint32_t kv_seq = 0, it_count = 0;
+    uint32_t q_arm[2] = {0, 0}, k_arm[4] = {0, 0, 0, 0}, v_arm[4] = {0, 0, 0, 0};
+    bool skip_pending = lead && p.inject_skip_first_kv != 0;
+    bool ok = true;
+    int item = first;
+    Quad it = item < total_items ? load_quad(p, item) : Quad{};
+    for (; ok && item < total_items; item += stride, ++it_count) {
+      const Quad nxt = item + stride < total_items ? load_quad(p, item + stride) : it;
+      const int nA = it.n_anchor_tiles();
+      const int n_tiles = it.n_tiles();
+      const bool sh = it.sfx_shared();
+      const int g = it.ag % hkv;
+      const uint64_t sfx_pol = it.n_sfx_tiles() > 1 ? keep : stream_pol;
+      for (int pos = 0; pos < n_tiles; ++pos, ++kv_seq) {
+        const int slot = kv_seq % C::kStages;
+        const uint32_t ph = (kv_seq / C::kStages) & 1u;
+        const CUtensorMap* mk;
+        const CUtensorMap* mv;
+        int row;
+        uint64_t pol;
+        if (pos < nA) {
+          mk = &maps.k_anc64;
+          mv = &maps.v_anc;
+          row = it.a_tok0 + pos * kBN;
+          pol = keep;
+        } else {
+          const int rel = pos - nA;
+          mk = &maps.k_suf64;
+          mv = &maps.v_suf;
+          row = sh ? it.wsp[0] + rel * kBN : it.wsp[rel & 1] + (rel >> 1) * kBN;
+          pol = sfx_pol;
+        }
+        uint8_t* k_dst = sKV + slot * C::kStageBytes;
+        uint8_t* v_dst = k_dst + C::kKHalfBytes;
+        if (!(ok = wait_parity_warp(wc, &bars->k_empty[slot], ph ^ 1u))) break;
+        if (skip_pending) {
+          skip_pending = false;  // fault injection: this K half never arrives
+        } else {
+          if (lead) ++k_arm[slot];
+          if (elect) {
+            if (lead) mbar_arrive_expect_tx(&bars->k_full[slot], 2 * C::kKHalfBytes);
+            for (int kb = 0; kb < C::kKB; ++kb)
+              tma_load_3d_pair(mk, lead_bar(&bars->k_full[slot]), k_dst + kb * C::kKHalfBlock,
+                               kb * 64, g, row + 64 * static_cast<int>(rank), pol);
+          }
+          __syncwarp();
+        }
+        if (pos == 0) {
+          for (int q = 0; q < 2 && ok; ++q) {
+            if (!(ok = wait_parity_warp(wc, &bars->q_empty[q], (it_count & 1u) ^ 1u)))
+              break;
+            if (lead) ++q_arm[q];
+            if (elect) {
+              if (lead) mbar_arrive_expect_tx(&bars->q_full[q], 2 * C::kQTileBytes);
+              for (int kb = 0; kb < C::kKB; ++kb)
+                tma_load_3d_pair(&maps.q, lead_bar(&bars->q_full[q]),
+                                 sQ + q * C::kQTileBytes + kb * C::kBlockBytes, kb * 64, g * G,
+                                 it.t0 + (2 * q + static_cast<int>(rank)) * tok, stream_pol);
+            }
+            __syncwarp();
+          }
+          if (!ok) break;
+        }
+        if (!(ok = wait_parity_warp(wc, &bars->v_empty[slot], ph ^ 1u))) break;
+        if (lead) ++v_arm[slot];
+        if (elect) {
+          if (lead) mbar_arrive_expect_tx(&bars->v_full[slot], 2 * C::kVHalfBytes);
+          tma_load_3d_pair(mv, lead_bar(&bars->v_full[slot]), v_dst,
+                           64 * static_cast<int>(rank), g, row, pol);
+        }
+        __syncwarp();
+      }
+      it = nxt;
+    }
+    // rank 0: every load of the pair that was issued has landed before the CTAs exit
+    // (rank 1's loads complete on rank 0's barriers)
+    if (lead) {
+      const uint64_t dl = global_timer_ns() + 100000000ull;
+      for (int q = 0; q < 2; ++q)
+        if (q_arm[q]) drain_wait(&bars->q_full[q], (q_arm[q] - 1) & 1u, dl);
+      for (int s = 0; s < C::kStages; ++s) {
+        if (k_arm[s]) drain_wait(&bars->k_full[s], (k_arm[s] - 1) & 1u, dl);
+        if (v_arm[s]) drain_wait(&bars->v_full[s], (v_arm[s] - 1) & 1u, dl);
+      }
+    }
+   } else if (warp == kWarpFillCheck && lead) {
+    // rank 0: the fill checker, as in the single-CTA kernel, on rank 0's full barriers
+    uint32_t kv_base = 0, arrived[2] = {0, 0};
+    bool ok = true;
+    int item = first;
+    Quad it = item < total_items ? load_quad(p, item) : Quad{};
+    for (; ok && item < total_items; item += stride) {
+      const Quad nxt = item + stride < total_items ? load_quad(p, item + stride) : it;
+      const int nA = it.n_anchor_tiles();
+      const int n = nA + it.n_sfx_tiles();
+      const bool sh = it.sfx_shared();
+      for (int k = 0; ok && k < n; ++k) {
+        for (int q = 0; ok && q < 2; ++q) {
+          if ((k >= nA && !sh) || q == 0) {
+            const uint32_t seq = kv_base + pos_of(nA, sh, q, k);
+            ok = wait_parity_warp(wc, &bars->v_full[seq % C::kStages], (seq / C::kStages) & 1u);
+          }
+          if (ok && k + 1 < n && ((k + 1 >= nA && !sh) || q == 0)) {
+            const uint32_t seq = kv_base + pos_of(nA, sh, q, k + 1);
+            ok = wait_parity_warp(wc, &bars->k_full[seq % C::kStages], (seq / C::kStages) & 1u);
+          }
+          if (ok && arrived[q] > 0)
+            ok = wait_parity_warp(wc, &bars->p_full[q], (arrived[q] - 1) & 1u);
+          if (!ok) break;
+          ++arrived[q];
+          if (lane == 0) mbar_arrive(&bars->p_full[q]);
+          __syncwarp();
+        }
+      }
+      kv_base += it.n_tiles();
+      it = nxt;
+    }
+   } else if (warp == kWarpMma && lead) {
+    // rank 0: every MMA of the pair
+    const bool elect = elect_one();
+    constexpr uint32_t kAB = 1u;  // bf16 A and B
+    constexpr uint32_t kIdescS = idesc_f16(256, 128, kAB, 0);
+    constexpr uint32_t kIdescPV = idesc_f16(256, D, kAB, 1);
+    constexpr uint32_t kDescHi = sw128_desc_hi(1024);  // 8-row groups 1024 bytes apart
+    const uint32_t q_lo0 = sw128_desc_lo(smem_u32(sQ), 16);
+    const uint32_t k_lo0 = sw128_desc_lo(smem_u32(sKV), 16);
+    // each CTA's V half is one 64-column block (128 rows x 128 bytes)
+    const uint32_t v_lo0 = sw128_desc_lo(smem_u32(sKV + C::kKHalfBytes), C::kBlockBytes);
+    uint32_t kv_base = 0, it_count = 0;
+    uint32_t p_cnt[2] = {0, 0};
+    bool ok = true;
+    int item = first;
+    Quad it = item < total_items ? load_quad(p, item) : Quad{};
+    for (; ok && item < total_items; item += stride, ++it_count) {
+      const Quad nxt = item + stride < total_items ? load_quad(p, item + stride) : it;
+      const int nA = it.n_anchor_tiles();
+      const int n = nA + it.n_sfx_tiles();
+      const bool sh = it.sfx_shared();
+      auto wait_s = [&](int q, int k) -> bool {
+        const uint32_t seq = kv_base + pos_of(nA, sh, q, k);
+        const bool own = k >= nA && !sh;
+        if ((own || q == 0) &&
+            !wait_parity_warp(wc, &bars->k_full[seq % C::kStages], (seq / C::kStages) & 1u))
+          return false;
+        if (k == 0 && !wait_parity_warp(wc, &bars->q_full[q], it_count & 1u)) return false;
+        return true;
+      };
+      auto wait_pv = [&](int q) -> bool {
+        if (!wait_parity_warp(wc, &bars->p_full[q], p_cnt[q] & 1u)) return false;
+        ++p_cnt[q];
+        return true;
+      };
+      auto mma_s = [&](int q, int k) {
+        const uint32_t seq = kv_base + pos_of(nA, sh, q, k);
+        const int slot = seq % C::kStages;
+        const uint32_t k_lo = k_lo0 + slot * (C::kStageBytes >> 4);
+        const uint32_t q_lo = q_lo0 + q * (C::kQTileBytes >> 4);
+        const uint32_t d_s = tmem + 256u * q;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          // K step kk: 128-byte block kk / 4 (16 KB apart for Q, 8 KB for the K half),
+          // 32-byte column offset (kk % 4) inside it
+          const uint32_t a_adv = (kk >> 2) * (C::kBlockBytes >> 4) + (kk & 3) * 2;
+          const uint32_t b_adv = (kk >> 2) * (C::kKHalfBlock >> 4) + (kk & 3) * 2;
+          mma_pair_ss(d_s, q_lo + a_adv, kDescHi, k_lo + b_adv, kDescHi, kIdescS,
+                      kk > 0 ? 1u : 0u);
+        }
+        mma_commit_pair(&bars->s_full[q]);
+        if ((k >= nA && !sh) || q == 1) mma_commit_pair(&bars->k_empty[slot]);
+        if (k == n - 1) mma_commit_pair(&bars->q_empty[q]);
+      };
+      auto mma_pv = [&](int q, int k) {
+        const uint32_t seq = kv_base + pos_of(nA, sh, q, k);
+        const int slot = seq % C::kStages;
+        const uint32_t v_lo = v_lo0 + slot * (C::kStageBytes >> 4);
+        const uint32_t d_o = tmem + 256u * q + 128u;
+        const uint32_t a_p = tmem + 256u * q + 64u;  // P over the upper half of S's columns
+        const uint32_t acc0 = k > 0 ? 1u : 0u;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_pair_ts(d_o, a_p + 8u * kk, v_lo + kk * 128, kDescHi, kIdescPV,
+                      kk > 0 ? 1u : acc0);
+        if ((k >= nA && !sh) || q == 1) mma_commit_pair(&bars->v_empty[slot]);
+        if (k == n - 1) mma_commit_pair(&bars->o_done[q]);
+      };
+      for (int q = 0; q < 2 && ok; ++q) {
+        ok = wait_s(q, 0);
+        if (ok) {
+          tc_fence_after();
+          if (elect) mma_s(q, 0);
+          __syncwarp();
+        }
+      }
+      for (int k = 0; ok && k < n; ++k) {
+        for (int q = 0; q < 2 && ok; ++q) {
+          ok = wait_pv(q);
+          if (!ok) break;
+          tc_fence_after();
+          if (elect) {
+            mma_pv(q, k);
+            if (k + 1 < n) mma_s(q, k + 1);
+          }
+          __syncwarp();
+        }
+      }
+      kv_base += it.n_tiles();
+      it = nxt;
+    }
+    if (elect) mma_commit_pair_local(&bars->drain);
+    __syncwarp();
+    drain_wait(&bars->drain, 0, global_timer_ns() + 100000000ull);
+   }
+  } else {
+    // ------------------------------------------------------ softmax warpgroups (both CTAs)
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg<D>::kRegsSoftmax));
+    const int q = warp >> 2;                        // pair tile
+    const int j = 2 * q + static_cast<int>(rank);   // query tile of the quad
+    const int row = threadIdx.x & 127;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + 256u * q;
+    const uint32_t t_o = t_s + 128u;
+    const uint32_t p_full_lead = lead_bar(&bars->p_full[q]);
+    uint32_t s_cnt = 0, it_count = 0;
+    bool ok = true;
+    const float c = p.scale_log2;
+    int item = first;
+    Quad it = item < total_items ? load_quad(p, item) : Quad{};
+    for (; ok && item < total_items; item += stride, ++it_count) {
+      const Quad nxt = item + stride < total_items ? load_quad(p, item + stride) : it;
+      const int nA = it.n_anchor_tiles();
+      const int n = nA + it.n_sfx_tiles();
+      const int g = it.ag % hkv;
+      const int t = it.t0 + j * tok + row / G;
+      const bool valid = t < it.tend[j];
+      const int vis_lo = valid ? __ldg(p.seg + t) : t;  // visible suffix keys: [vis_lo, t]
+      const int ws_q = it.wsp[q];
+      const float c_anc = FP8 ? c * __ldg(p.k_scale + it.ag) : c;
+      const float v_sc = FP8 ? __ldg(p.v_scale + it.ag) : 1.0f;
+      float m_ref = 0.0f, l = 0.0f;
+      for (int k = 0; k < n; ++k) {
+        if (!(ok = wait_parity(wc, &bars->s_full[q], s_cnt & 1u))) break;
+        ++s_cnt;
+        tc_fence_after();
+        if (k < nA) {
+          const int rem = it.la - k * kBN;
+          softmax_tile_spec<128, FP8>(t_s, k == 0, rem < kBN, 0, rem - 1, c_anc, v_sc, m_ref, l);
+        } else {
+          const int base = ws_q + (k - nA) * kBN;
+          const int lo_c = vis_lo - base, hi_c = t - base;
+          const bool mk = __any_sync(0xFFFFFFFFu, lo_c > 0 || hi_c < kBN - 1);
+          softmax_tile_spec<128, false>(t_s, k == 0, mk, lo_c, hi_c, c, 1.0f, m_ref, l);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(p_full_lead);
+      }
+      if (!ok) break;
+      // a valid row outside the fast-kernel bounds: the quad's non-empty halves go to the
+      // exact kernel (as items 2 x quad and 2 x quad + 1)
+      const bool broke = !(l >= kSpecSumLow && l <= kSpecSumHigh) ||
+                         (FP8 && it.la > 0 && !(fabsf(v_sc) <= kSpecScaleHigh));
+      if (__any_sync(0xFFFFFFFFu, broke && valid) && lane == 0) {
+        if (atomicExch(p.redo_flag + item, 1) == 0) {
+          const bool half1 = it.tend[2] > it.t0 + 2 * tok;
+          const int at = atomicAdd(p.redo_count, half1 ? 2 : 1);
+          p.redo_list[at] = 2 * item;
+          if (half1) p.redo_list[at + 1] = 2 * item + 1;
+        }
+      }
+      __syncwarp();
+      if (!(ok = wait_parity(wc, &bars->o_done[q], it_count & 1u))) break;
+      tc_fence_after();
+      const float inv_l = 1.0f / l;
+      const uint64_t il = f2(inv_l, inv_l);
+      const int64_t orow = static_cast<int64_t>(t) * p.hq + g * G + (row % G);
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + orow * D;
+#pragma unroll
+      for (int ch2 = 0; ch2 < D / 64; ++ch2) {
+        uint32_t r[2][32];
+        tmem_ld32(t_o + ch2 * 64, r[0]);
+        tmem_ld32(t_o + ch2 * 64 + 32, r[1]);
+        tmem_wait_ld_dep(r[0]);
+        reg_dep(r[1]);
+        if (valid) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              float lo, hi;
+              f2_split(f2_mul(f2(__uint_as_float(r[h][2 * e]), __uint_as_float(r[h][2 * e + 1])),
+                              il),
+                       lo, hi);
+              pk[e] = pack_bf16(lo, hi);
+            }
+            st_global_v8(out + ch2 * 64 + h * 32, pk);
+            st_global_v8(out + ch2 * 64 + h * 32 + 16, pk + 8);
+          }
+        }
+      }
+      if (valid && p.lse != nullptr)
+        p.lse[orow] = (m_ref + __log2f(l)) * 0.69314718055994531f;
+      it = nxt;
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  // Each CTA tells the other whether it gave up on a wait. Rank 1's copies complete on
+  // rank 0's barriers, and after an abort nothing waits for those that were issued: then
+  // both CTAs give copies in flight 50 us to land before either exits.
+  if (threadIdx.x == 0 && bars->abort_flag)
+    st_cluster_u32(cluster_map(&bars->peer_abort, rank ^ 1u), 1u);
+  cluster_sync();  // also: rank 0's MMAs on rank 1's shared memory and TMEM are complete
+  if (bars->abort_flag || bars->peer_abort) {
+    const uint64_t until = global_timer_ns() + 50000ull;
+    while (global_timer_ns() < until) {
+    }
+    __syncthreads();
+    cluster_sync();
+  }
+  if (warp == kWarpMma) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------------------------
 // Per-suffix offset checks and the per-token suffix start. Each suffix is checked on its
 // own (0 <= start <= end <= T_S, length <= max_suffix_len) before any write, so nothing
@@ -996,7 +1480,7 @@ __global__ void __launch_bounds__(1024) cascade_schedule_kernel(const CascadePar
     for (int i = tid; i <= A; i += blockDim.x) prefix[i] = 0;
     return;
   }
-  const int pair_tok = 2 * p.tok_per_tile;
+  const int pair_tok = p.tiles_per_item * p.tok_per_tile;  // suffix tokens per work item
   for (int a = tid; a < A; a += blockDim.x) {
     const int key = min((ao[a + 1] - ao[a] + kBN - 1) / kBN, kSortBins - 1);
     atomicAdd(&hist[kSortBins - 1 - key], 1);
@@ -1034,7 +1518,9 @@ __global__ void __launch_bounds__(1024) cascade_schedule_kernel(const CascadePar
   if (tid == 0) prefix[A] = carry;
 }
 
-// One record per work item: (a_tok0, la, t0, a * Hkv + g, ws0, ws1, tend0, tend1).
+// One record per work item: (a_tok0, la, t0, a * Hkv + g, ws0, ws1, tend0, tend1); for
+// the CTA-pair kernel one per quad: (a_tok0, la, t0, a * Hkv + g, wsp0, wsp1, tend0,
+// tend1, tend2, tend3).
 __global__ void __launch_bounds__(256) cascade_items_kernel(const CascadeParams p) {
   const int item = blockIdx.x * blockDim.x + threadIdx.x;
   const int A = p.num_anchors;
@@ -1051,6 +1537,23 @@ __global__ void __launch_bounds__(256) cascade_items_kernel(const CascadeParams 
   const int s_begin = p.suffix_offsets[p.anchor_suffix_ptr[a]];
   const int s_end = p.suffix_offsets[p.anchor_suffix_ptr[a + 1]];
   const int tok = p.tok_per_tile;
+  if (p.tiles_per_item == 4) {
+    const int quads = (s_end - s_begin + 4 * tok - 1) / (4 * tok);
+    const int g = local / quads;
+    const int t0 = s_begin + (local % quads) * 4 * tok;
+    int tend[4];
+    for (int j = 0; j < 4; ++j) {
+      const int start = t0 + j * tok;
+      tend[j] = start < s_end ? min(start + tok, s_end) : start;
+    }
+    int4* dst = reinterpret_cast<int4*>(p.items + 12 * static_cast<int64_t>(item));
+    dst[0] = make_int4(p.anchor_offsets[a], p.anchor_offsets[a + 1] - p.anchor_offsets[a], t0,
+                       a * p.hkv + g);
+    const int s2 = t0 + 2 * tok;
+    dst[1] = make_int4(p.seg[t0], s2 < s_end ? p.seg[s2] : s2, tend[0], tend[1]);
+    dst[2] = make_int4(tend[2], tend[3], 0, 0);
+    return;
+  }
   const int pairs = (s_end - s_begin + 2 * tok - 1) / (2 * tok);
   const int g = local / pairs;
   const int t0 = s_begin + (local % pairs) * 2 * tok;
@@ -1268,7 +1771,7 @@ CascadeWorkspace cascade_workspace_layout(int num_anchors, int64_t total_suffix_
   w.order = w.prefix + 4 * (static_cast<size_t>(num_anchors) + 1);
   w.seg = up(w.order + 4 * static_cast<size_t>(num_anchors), 16);
   w.items = up(w.seg + 4 * static_cast<size_t>(total_suffix_tokens), 32);
-  w.redo_flag = w.items + 32 * static_cast<size_t>(item_bound);
+  w.redo_flag = w.items + 48 * static_cast<size_t>(item_bound);  // records of up to 12 ints
   w.redo_list = w.redo_flag + 4 * static_cast<size_t>(item_bound);
   w.k_anc_bf16 = up(w.redo_list + 4 * static_cast<size_t>(item_bound), 256);
   w.v_anc_bf16 = up(w.k_anc_bf16 + static_cast<size_t>(anchor_bf16_bytes), 256);
@@ -1297,15 +1800,63 @@ static cudaError_t launch_attn_kernel(const CascadeParams& p, const CascadeMaps&
   return cudaGetLastError();
 }
 
-// The fast kernel, then the exact kernel over the items it handed over (none: its CTAs
-// return at once).
+// Clusters of two CTAs (one per SM) that can be resident at once, per device.
+template <bool FP8>
+static int pair_clusters(int num_sms, cudaStream_t stream) {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::atomic<int>* slot = dev >= 0 && dev < 64 ? &cache[dev] : nullptr;
+  if (slot != nullptr && slot->load() > 0) return slot->load();
+  int clusters = 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(num_sms / 2 * 2), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = PairCfg::kSmemBytes;
+  cfg.stream = stream;
+  if (cudaOccupancyMaxActiveClusters(&clusters, cascade_pair_kernel<FP8>, &cfg) != cudaSuccess ||
+      clusters <= 0) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (slot != nullptr) slot->store(clusters);
+  return clusters;
+}
+
+template <bool FP8>
+static cudaError_t launch_pair_kernel(const CascadeParams& p, const CascadeMaps& maps,
+                                      int num_sms, cudaStream_t stream) {
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, cascade_pair_kernel<FP8>);
+  if (e != cudaSuccess) return e;
+  if (static_cast<int64_t>(attr.numRegs) * kThreads <
+      256 * Cfg<128>::kRegsSoftmax + 128 * Cfg<128>::kRegsOther)
+    return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(cascade_pair_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           PairCfg::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int clusters = pair_clusters<FP8>(num_sms, stream);
+  if (clusters <= 0) return cudaErrorInvalidConfiguration;
+  // quads <= item_bound (the bound on two-tile items)
+  const int grid = 2 * (p.item_bound < clusters ? p.item_bound : clusters);
+  if (grid <= 0) return cudaSuccess;
+  cascade_pair_kernel<FP8><<<grid, kThreads, PairCfg::kSmemBytes, stream>>>(p, maps);
+  return cudaGetLastError();
+}
+
+// The fast kernel (single CTAs, or CTA pairs over quads), then the exact kernel over the
+// items it handed over (none: its CTAs return at once).
 template <int D, bool FP8>
 static cudaError_t launch_attn_d(const CascadeParams& p, const CascadeMaps& maps, int num_sms,
                                  cudaStream_t stream) {
   // the K/V amax (causal prefill) is formed by the fast kernel, which sees every item
   const bool amax = !FP8 && p.k_amax != nullptr;
-  cudaError_t e = amax ? launch_attn_kernel<D, false, false, true>(p, maps, num_sms, stream)
-                       : launch_attn_kernel<D, FP8, false>(p, maps, num_sms, stream);
+  cudaError_t e;
+  if (D == 128 && p.tiles_per_item == 4)
+    e = launch_pair_kernel<FP8>(p, maps, num_sms, stream);
+  else
+    e = amax ? launch_attn_kernel<D, false, false, true>(p, maps, num_sms, stream)
+             : launch_attn_kernel<D, FP8, false>(p, maps, num_sms, stream);
   if (e != cudaSuccess) return e;
   e = launch_attn_kernel<D, FP8, true>(p, maps, num_sms, stream);
   if (e != cudaSuccess || !amax || p.num_suffixes == 0) return e;
@@ -1315,8 +1866,26 @@ static cudaError_t launch_attn_d(const CascadeParams& p, const CascadeMaps& maps
   return cudaGetLastError();
 }
 
-cudaError_t launch_cascade(const CascadeParams& p, const CascadeMaps& maps, int head_dim,
+namespace {
+std::atomic<int> g_cta_pairs{QUAIL_CTA_PAIRS_AUTO};
+}
+void set_cta_pairs(int mode) { g_cta_pairs.store(mode); }
+
+cudaError_t launch_cascade(const CascadeParams& params, const CascadeMaps& maps, int head_dim,
                            bool fp8, int num_sms, cudaStream_t stream) {
+  // The CTA-pair kernel takes d = 128 calls with both parts fused and no K/V amax (the
+  // fault-injection switch exercises the single-CTA kernel's timeout path). Automatic
+  // choice: a pair tile's suffix window spans two query tiles and is loaded as 128-key
+  // tiles, while the single-CTA kernel loads a window of at most 64 keys as one 64-key
+  // tile; when every query tile's window fits in 64 keys (tokens per tile + the longest
+  // suffix - 1 <= 64: short suffixes, many per tile) the pair would do more work on the
+  // suffix part than it saves, and the single-CTA kernel runs.
+  CascadeParams p = params;
+  const int mode = g_cta_pairs.load();
+  bool pairs = mode != QUAIL_CTA_PAIRS_OFF && head_dim == 128 && p.mode == kFused &&
+               p.k_amax == nullptr && p.inject_skip_first_kv == 0 && num_sms >= 2;
+  if (mode == QUAIL_CTA_PAIRS_AUTO && p.tok_per_tile + p.max_suffix_len - 1 <= 64) pairs = false;
+  p.tiles_per_item = pairs ? 4 : 2;
   cudaError_t e = cudaMemsetAsync(p.flag, 0, sizeof(int32_t), stream);
   if (e != cudaSuccess) return e;
   if (p.num_suffixes > 0) {

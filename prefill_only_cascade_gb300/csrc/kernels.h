@@ -92,7 +92,7 @@ struct CascadeParams {
   int32_t* prefix;           // [A+1] work-item prefix over the anchor order; [A] = total
   int32_t* order;            // [A] anchors by decreasing anchor-tile count
   int32_t* seg;              // [T_S] first token of the suffix that holds each token
-  int32_t* items;            // [item_bound][8] one record per work item
+  int32_t* items;            // [item_bound][12] one record per work item (8 or 12 ints)
   int32_t* redo_count;       // items the speculative kernel handed to the exact one
   int32_t* redo_flag;        // [item_bound] nonzero: item is in redo_list
   int32_t* redo_list;        // [item_bound] item indices, redo_count of them valid
@@ -106,6 +106,9 @@ struct CascadeParams {
   //                the LSE merge with (o_part, lse_part) done in the epilogue
   int mode;
   int merge;
+  // 2: work items of two 128-row query tiles (one CTA each); 4: "quads" of four query
+  // tiles for the CTA-pair kernel (the exact kernel then walks quad halves)
+  int tiles_per_item;
   float* o_part;             // [T_S, Hq, D] fp32
   float* lse_part;           // [T_S, Hq] fp32 (natural log)
   // Optional (causal prefill): max |x| of the suffix K and V per (suffix, KV head),
@@ -133,7 +136,12 @@ int64_t cascade_item_bound(int num_anchors, int64_t total_suffix_tokens, int hkv
 // Tensor maps over q_suf, k/v anchor and k/v suffix (bf16, 3-D: d, head, token).
 struct CascadeMaps {
   CUtensorMap q, k_anc, v_anc, k_suf, v_suf;
+  CUtensorMap k_anc64, k_suf64;  // the same K tensors with 64-row boxes (CTA-pair halves)
 };
+
+// Which d = 128 fused calls run the CTA-pair kernel: QUAIL_CTA_PAIRS_OFF / _AUTO (the
+// default) / _ALWAYS.
+void set_cta_pairs(int mode);
 
 constexpr int kFused = 0, kAnchorPass = 1, kSuffixPass = 2;
 

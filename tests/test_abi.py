@@ -211,3 +211,11 @@ def test_quantize_with_scales_rejects_bad_arguments():
     assert call(amax=None) == q.QUAIL_ERR_INVALID_ARG
     assert call(amax=ctypes.c_void_p(0x10002)) == q.QUAIL_ERR_INVALID_ARG
     assert call(x=ctypes.c_void_p(0x10008)) == q.QUAIL_ERR_INVALID_ARG
+
+
+def test_cta_pair_mode_values_checked():
+    # host-only: the mode switch validates its argument (no kernel runs)
+    assert q.set_cta_pairs(3) == q.QUAIL_ERR_INVALID_ARG
+    assert q.set_cta_pairs(-1) == q.QUAIL_ERR_INVALID_ARG
+    for mode in (q.CTA_PAIRS_OFF, q.CTA_PAIRS_ALWAYS, q.CTA_PAIRS_AUTO):
+        assert q.set_cta_pairs(mode) == q.QUAIL_OK
