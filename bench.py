@@ -88,9 +88,18 @@ def attention_bytes(layout, hq, hkv, d, kv_bytes=2) -> float:
                  + 4 * (2 * (layout.num_anchors + 1) + layout.num_suffixes + 1))
 
 
+def pair_kernel(layout, hq, hkv, d) -> bool:
+    """Whether quail_cascade_attn's automatic choice runs the CTA-pair kernel for this
+    layout: d = 128 and some query tile's suffix window can exceed 64 keys (128 / G
+    tokens a tile + the longest suffix - 1 > 64); the rule the library states for
+    QUAIL_CTA_PAIRS_AUTO."""
+    return d == 128 and (128 // (hq // hkv)) + int(layout.max_suffix_len) - 1 > 64
+
+
 def work_items(layout, hkv, group) -> int:
     """Work items of one cascade call: per anchor and KV head, one per pair of 128-row
-    query tiles over the anchor's suffix tokens (bench bookkeeping for the redo rate)."""
+    query tiles over the anchor's suffix tokens (bench bookkeeping for the redo rate; a
+    CTA-pair quad counts as its two halves, as the exact kernel's list does)."""
     pair_tok = 2 * (128 // group)
     so, asp = layout.suffix_offsets.astype(np.int64), layout.anchor_suffix_ptr.astype(np.int64)
     ntok = so[asp[1:]] - so[asp[:-1]]
@@ -549,15 +558,19 @@ def measure_attention(q, cfg, layout, dev, args, *, steps, e2e=False, cpu_budget
     achieved_tflops = flops / (attn_ms / 1e3) / 1e12
     peak = pk["bf16_tflops"]
     abytes = attention_bytes(layout, hq, hkv, d, 1 if kv_fp8 else 2)
-    traffic = traffic_from_profile("cascade.cu", f"cascade_attn_{cfg.name}.md")
+    traffic = traffic_from_profile(
+        "cascade.cu", ("cascade_pair_" if pair_kernel(layout, hq, hkv, d) else "cascade_attn_") +
+        f"{cfg.name}.md")
     roofline = {"bound": "tensor", "achieved": round(achieved_tflops, 2), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved_tflops / peak, 4),
                 "traffic": traffic, "peak_source": f"bf16_tflops (burst) of {src}",
                 "frac_of_sustained": (round(achieved_tflops / pk["bf16_tflops_sustained"], 4)
                                       if "bf16_tflops_sustained" in pk else None),
-                "kernel": "cascade_attn_kernel, fast + exact launches (+ its 3 schedule "
-                          "kernels" + (" and the e4m3 -> bf16 anchor staging kernel"
-                                       if kv_fp8 else "") + "): one quail_cascade_attn call",
+                "kernel": (("cascade_pair_kernel (CTA pairs)" if pair_kernel(layout, hq, hkv, d)
+                            else "cascade_attn_kernel") + " fast launch + the exact launch "
+                           "(+ 3 schedule kernels" +
+                           (" and the e4m3 -> bf16 anchor staging kernel" if kv_fp8 else "") +
+                           "): one quail_cascade_attn call"),
                 "kernel_ms": round(attn_ms, 4),
                 "algorithmic_flops_per_launch": flops,
                 "algorithmic_bytes_per_launch": abytes,

@@ -97,7 +97,7 @@ struct Cfg {
   static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= 384 * 168, "register split");
 };
 struct __align__(8) Bars {
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[4], q_empty[4];  // the single-CTA kernel uses [0, 2)
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t drain;
@@ -141,8 +141,11 @@ __device__ __forceinline__ int4 ld_nc_v4(const int32_t* p) {
   return v;
 }
 
+// QUADS: the caller may walk quad halves (the exact kernel; the fast single-CTA kernel
+// always runs with two-tile items, and leaves the branch out).
+template <bool QUADS>
 __device__ __forceinline__ Item load_item(const CascadeParams& p, int item) {
-  if (p.tiles_per_item == 4) {
+  if (QUADS && p.tiles_per_item == 4) {
     // half h of quad item / 2 (the exact kernel after the CTA-pair kernel): its query
     // tiles 2h and 2h + 1, each with its own key window
     const int quad = item >> 1, h = item & 1;
@@ -472,7 +475,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       // before the slot is overwritten.
       uint32_t pend_k = 0, pend_v = 0;
       auto landed = [&](uint64_t* bar, uint32_t parity) {
-        return __shfl_sync(0xFFFFFFFFu, mbar_try_wait(smem_u32(bar), parity) ? 1 : 0, 0) != 0;
+        return __shfl_sync(0xFFFFFFFFu, mbar_test_wait(smem_u32(bar), parity) ? 1 : 0, 0) != 0;
       };
       auto service = [&]() {
         if constexpr (AMAX) {
@@ -489,9 +492,9 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         }
       };
       int item = blockIdx.x;
-      Item it = item < total_items ? load_item(p, item_id(item)) : Item{};
+      Item it = item < total_items ? load_item<EXACT>(p, item_id(item)) : Item{};
       for (; ok && item < total_items; item += stride, ++it_count) {
-        const Item nxt = item + stride < total_items ? load_item(p, item_id(item + stride)) : it;
+        const Item nxt = item + stride < total_items ? load_item<EXACT>(p, item_id(item + stride)) : it;
         const int nA = it.n_anchor_tiles();
         const int n_tiles = it.n_tiles();
         const bool sh = it.sfx_shared();
@@ -619,9 +622,9 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
     uint32_t kv_base = 0, arrived[2] = {0, 0};
     bool ok = true;
     int item = blockIdx.x;
-    Item it = item < total_items ? load_item(p, item_id(item)) : Item{};
+    Item it = item < total_items ? load_item<EXACT>(p, item_id(item)) : Item{};
     for (; ok && item < total_items; item += stride) {
-      const Item nxt = item + stride < total_items ? load_item(p, item_id(item + stride)) : it;
+      const Item nxt = item + stride < total_items ? load_item<EXACT>(p, item_id(item + stride)) : it;
       const int nA = it.n_anchor_tiles();
       const int nS = it.n_sfx_tiles();
       const int n = nA + nS;
@@ -665,9 +668,9 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       uint32_t p_cnt[2] = {0, 0};
       bool ok = true;
       int item = blockIdx.x;
-      Item it = item < total_items ? load_item(p, item_id(item)) : Item{};
+      Item it = item < total_items ? load_item<EXACT>(p, item_id(item)) : Item{};
       for (; ok && item < total_items; item += stride, ++it_count) {
-        const Item nxt = item + stride < total_items ? load_item(p, item_id(item + stride)) : it;
+        const Item nxt = item + stride < total_items ? load_item<EXACT>(p, item_id(item + stride)) : it;
         const int nA = it.n_anchor_tiles();
         const int nS = it.n_sfx_tiles();
         const int nk_sfx = it.nk_sfx();
@@ -781,9 +784,9 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
     bool ok = true;
     const float c = p.scale_log2;
     int item = blockIdx.x;
-    Item it = item < total_items ? load_item(p, item_id(item)) : Item{};
+    Item it = item < total_items ? load_item<EXACT>(p, item_id(item)) : Item{};
     for (; ok && item < total_items; item += stride, ++it_count) {
-      const Item nxt = item + stride < total_items ? load_item(p, item_id(item + stride)) : it;
+      const Item nxt = item + stride < total_items ? load_item<EXACT>(p, item_id(item + stride)) : it;
       const int nA = it.n_anchor_tiles();
       const int n = nA + it.n_sfx_tiles();
       const int nk_sfx = it.nk_sfx();
@@ -960,24 +963,32 @@ struct PairCfg {
   static constexpr int kKHalfBytes = 2 * kKHalfBlock;    // 64 keys x d
   static constexpr int kVHalfBytes = kBlockBytes;        // 128 keys x 64 d columns
   static constexpr int kStageBytes = kKHalfBytes + kVHalfBytes;
+  // Query-tile buffers: query tile qq of the quad with walk count ic is query slot
+  // j = 2 ic + qq, held in buffer j % kQBufs (its use j / kQBufs). A third or fourth
+  // buffer (the next quad's queries loading a whole quad ahead, at the cost of a K/V
+  // stage) measured no faster, nor did an L2 prefetch of the next quad's query rows.
+  static constexpr int kQBufs = 2;
   static constexpr int kStages = 4;
-  static constexpr int kSmemQ = 2 * kQTileBytes;
+  static constexpr int kSmemQ = kQBufs * kQTileBytes;
   static constexpr int kSmemKV = kStages * kStageBytes;
   static constexpr int kSmemBytes = kSmemQ + kSmemKV + 1024 + 1024;
 };
 
 struct Quad {
   int a_tok0, la, t0, ag;
-  int wsp[2];   // key window start of pair tile 0 / 1 (start of the suffix of its first token)
-  int tend[4];  // one past the last token of query tile j (its start when empty)
+  int wsp0, wsp1;          // key window start of pair tile 0 / 1 (its first token's suffix)
+  int te0, te1, te2, te3;  // one past the last token of query tile j (its start when empty)
+  // selects, not indexing: a dynamically indexed array would live in local memory
+  __device__ __forceinline__ int wsp(int q) const { return q ? wsp1 : wsp0; }
+  __device__ __forceinline__ int tend(int j) const {
+    return j < 2 ? (j ? te1 : te0) : (j == 3 ? te3 : te2);
+  }
   __device__ __forceinline__ int n_anchor_tiles() const { return (la + kBN - 1) / kBN; }
-  __device__ __forceinline__ int window(int q) const {
-    return max(max(tend[2 * q], tend[2 * q + 1]) - wsp[q], 0);
-  }
   __device__ __forceinline__ int n_sfx_tiles() const {
-    return (max(window(0), window(1)) + kBN - 1) / kBN;
+    const int w = max(max(max(te0, te1) - wsp0, max(te2, te3) - wsp1), 0);
+    return (w + kBN - 1) / kBN;
   }
-  __device__ __forceinline__ bool sfx_shared() const { return wsp[0] == wsp[1]; }
+  __device__ __forceinline__ bool sfx_shared() const { return wsp0 == wsp1; }
   __device__ __forceinline__ int n_tiles() const {
     return n_anchor_tiles() + (sfx_shared() ? 1 : 2) * n_sfx_tiles();
   }
@@ -988,8 +999,8 @@ __device__ __forceinline__ Quad load_quad(const CascadeParams& p, int item) {
   const int4 c = ld_nc_v4(p.items + 12 * static_cast<int64_t>(item) + 8);
   Quad it;
   it.a_tok0 = a.x; it.la = a.y; it.t0 = a.z; it.ag = a.w;
-  it.wsp[0] = b.x; it.wsp[1] = b.y; it.tend[0] = b.z; it.tend[1] = b.w;
-  it.tend[2] = c.x; it.tend[3] = c.y;
+  it.wsp0 = b.x; it.wsp1 = b.y; it.te0 = b.z; it.te1 = b.w;
+  it.te2 = c.x; it.te3 = c.y;
   return it;
 }
 
@@ -1012,9 +1023,11 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
+    for (int b = 0; b < C::kQBufs; ++b) {
+      mbar_init(&bars->q_full[b], 1);
+      mbar_init(&bars->q_empty[b], 1);
+    }
     for (int q = 0; q < 2; ++q) {
-      mbar_init(&bars->q_full[q], 1);
-      mbar_init(&bars->q_empty[q], 1);
       mbar_init(&bars->s_full[q], 1);
       mbar_init(&bars->p_full[q], 9);  // 2 x 4 softmax warps + the fill checker
       mbar_init(&bars->o_done[q], 1);
@@ -1067,13 +1080,45 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
     }
     const uint64_t keep = l2_policy_evict_last(), stream_pol = l2_policy_evict_first();
     uint32_t kv_seq = 0, it_count = 0;
-    uint32_t q_arm[2] = {0, 0}, k_arm[4] = {0, 0, 0, 0}, v_arm[4] = {0, 0, 0, 0};
+    uint32_t q_arm[4] = {0, 0, 0, 0}, k_arm[4] = {0, 0, 0, 0}, v_arm[4] = {0, 0, 0, 0};
     bool skip_pending = lead && p.inject_skip_first_kv != 0;
     bool ok = true;
+    // Queries: query tile qq of the quad with walk count ic is query slot 2 ic + qq. Slots
+    // are issued strictly in order; n_issued counts them.
+    uint32_t n_issued = 0;
+    auto issue_q = [&](const Quad& x) {
+      const int qq = static_cast<int>(n_issued & 1u);
+      const int buf = static_cast<int>(n_issued % C::kQBufs);
+      ++n_issued;
+      if (lead) ++q_arm[buf];
+      if (elect) {
+        if (lead) mbar_arrive_expect_tx(&bars->q_full[buf], 2 * C::kQTileBytes);
+        for (int kb = 0; kb < C::kKB; ++kb)
+          tma_load_3d_pair(&maps.q, lead_bar(&bars->q_full[buf]),
+                           sQ + buf * C::kQTileBytes + kb * C::kBlockBytes, kb * 64,
+                           (x.ag % hkv) * G, x.t0 + (2 * qq + static_cast<int>(rank)) * tok,
+                           stream_pol);
+      }
+      __syncwarp();
+    };
+    // Whether the buffer of query slot j = n_issued is free, polled (warp-uniform). The
+    // parity test is exact only because slot j - kQBufs, the buffer's previous use, has been
+    // issued (in-order issue): the buffer's empty barrier is then at most one phase short
+    // of the release that slot j needs, never two (two short, the same parity would read
+    // as released).
+    auto next_slot_free = [&]() {
+      const uint32_t j = n_issued;
+      const int buf = static_cast<int>(j % C::kQBufs);
+      const uint32_t par = ((j / C::kQBufs) & 1u) ^ 1u;
+      return __shfl_sync(0xFFFFFFFFu, mbar_test_wait(smem_u32(&bars->q_empty[buf]), par) ? 1 : 0,
+                         0) != 0;
+    };
     int item = first;
     Quad it = item < total_items ? load_quad(p, item) : Quad{};
     for (; ok && item < total_items; item += stride, ++it_count) {
-      const Quad nxt = item + stride < total_items ? load_quad(p, item + stride) : it;
+      const bool has_next = item + stride < total_items;
+      const Quad nxt = has_next ? load_quad(p, item + stride) : it;
+      const uint32_t cur_end = 2 * it_count + 2;  // one past this quad's query slots
       const int nA = it.n_anchor_tiles();
       const int n_tiles = it.n_tiles();
       const bool sh = it.sfx_shared();
@@ -1095,7 +1140,7 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
           const int rel = pos - nA;
           mk = &maps.k_suf64;
           mv = &maps.v_suf;
-          row = sh ? it.wsp[0] + rel * kBN : it.wsp[rel & 1] + (rel >> 1) * kBN;
+          row = sh ? it.wsp0 + rel * kBN : it.wsp(rel & 1) + (rel >> 1) * kBN;
           pol = sfx_pol;
         }
         uint8_t* k_dst = sKV + slot * C::kStageBytes;
@@ -1113,22 +1158,20 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
           }
           __syncwarp();
         }
-        if (pos == 0) {
-          for (int q = 0; q < 2 && ok; ++q) {
-            if (!(ok = wait_parity_warp(wc, &bars->q_empty[q], (it_count & 1u) ^ 1u)))
+        if (pos == 0) {  // this quad's queries, unless they went out during the last quad
+          while (ok && n_issued < cur_end) {
+            const uint32_t j = n_issued;
+            const int buf = static_cast<int>(j % C::kQBufs);
+            if (!(ok = wait_parity_warp(wc, &bars->q_empty[buf], ((j / C::kQBufs) & 1u) ^ 1u)))
               break;
-            if (lead) ++q_arm[q];
-            if (elect) {
-              if (lead) mbar_arrive_expect_tx(&bars->q_full[q], 2 * C::kQTileBytes);
-              for (int kb = 0; kb < C::kKB; ++kb)
-                tma_load_3d_pair(&maps.q, lead_bar(&bars->q_full[q]),
-                                 sQ + q * C::kQTileBytes + kb * C::kBlockBytes, kb * 64, g * G,
-                                 it.t0 + (2 * q + static_cast<int>(rank)) * tok, stream_pol);
-            }
-            __syncwarp();
+            issue_q(it);
           }
           if (!ok) break;
         }
+        // the next quad's queries load while this one runs, as soon as their buffers are
+        // free (after this quad's own query slots, so in order)
+        while (has_next && n_issued < cur_end + 2 && n_issued >= cur_end && next_slot_free())
+          issue_q(nxt);
         if (!(ok = wait_parity_warp(wc, &bars->v_empty[slot], ph ^ 1u))) break;
         if (lead) ++v_arm[slot];
         if (elect) {
@@ -1144,8 +1187,8 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
     // (rank 1's loads complete on rank 0's barriers)
     if (lead) {
       const uint64_t dl = global_timer_ns() + 100000000ull;
-      for (int q = 0; q < 2; ++q)
-        if (q_arm[q]) drain_wait(&bars->q_full[q], (q_arm[q] - 1) & 1u, dl);
+      for (int b = 0; b < C::kQBufs; ++b)
+        if (q_arm[b]) drain_wait(&bars->q_full[b], (q_arm[b] - 1) & 1u, dl);
       for (int s = 0; s < C::kStages; ++s) {
         if (k_arm[s]) drain_wait(&bars->k_full[s], (k_arm[s] - 1) & 1u, dl);
         if (v_arm[s]) drain_wait(&bars->v_full[s], (v_arm[s] - 1) & 1u, dl);
@@ -1204,13 +1247,18 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
       const int nA = it.n_anchor_tiles();
       const int n = nA + it.n_sfx_tiles();
       const bool sh = it.sfx_shared();
+      // this quad's query buffers (query slots 2 it_count and 2 it_count + 1)
+      auto qbuf = [&](int q) { return static_cast<int>((2 * it_count + q) % C::kQBufs); };
+      auto quse = [&](int q) { return ((2 * it_count + q) / C::kQBufs) & 1u; };
       auto wait_s = [&](int q, int k) -> bool {
         const uint32_t seq = kv_base + pos_of(nA, sh, q, k);
         const bool own = k >= nA && !sh;
         if ((own || q == 0) &&
             !wait_parity_warp(wc, &bars->k_full[seq % C::kStages], (seq / C::kStages) & 1u))
           return false;
-        if (k == 0 && !wait_parity_warp(wc, &bars->q_full[q], it_count & 1u)) return false;
+        if (k == 0 &&
+            !wait_parity_warp(wc, &bars->q_full[qbuf(q)], quse(q)))
+          return false;
         return true;
       };
       auto wait_pv = [&](int q) -> bool {
@@ -1222,7 +1270,7 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
         const uint32_t seq = kv_base + pos_of(nA, sh, q, k);
         const int slot = seq % C::kStages;
         const uint32_t k_lo = k_lo0 + slot * (C::kStageBytes >> 4);
-        const uint32_t q_lo = q_lo0 + q * (C::kQTileBytes >> 4);
+        const uint32_t q_lo = q_lo0 + qbuf(q) * (C::kQTileBytes >> 4);
         const uint32_t d_s = tmem + 256u * q;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -1235,7 +1283,7 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
         }
         mma_commit_pair(&bars->s_full[q]);
         if ((k >= nA && !sh) || q == 1) mma_commit_pair(&bars->k_empty[slot]);
-        if (k == n - 1) mma_commit_pair(&bars->q_empty[q]);
+        if (k == n - 1) mma_commit_pair(&bars->q_empty[qbuf(q)]);
       };
       auto mma_pv = [&](int q, int k) {
         const uint32_t seq = kv_base + pos_of(nA, sh, q, k);
@@ -1291,19 +1339,62 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
     uint32_t s_cnt = 0, it_count = 0;
     bool ok = true;
     const float c = p.scale_log2;
+    // What this warp needs of a quad. The next quad's record is loaded at the start of the
+    // current one and decoded at its end: decoding it at once would wait for the load at
+    // the item boundary, on the critical path.
+    struct Part {
+      int nA, n, la, ag, t0, ws_q, tend_j;
+      bool half1;  // query tiles 2 and 3 are not empty
+    };
+    auto part_of = [&](int i, const Quad& x) {
+      Part r{};
+      if (i < total_items) {
+        r.nA = x.n_anchor_tiles();
+        r.n = r.nA + x.n_sfx_tiles();
+        r.la = x.la;
+        r.ag = x.ag;
+        r.t0 = x.t0;
+        r.ws_q = x.wsp(q);
+        r.tend_j = x.tend(j);
+        r.half1 = x.te2 > x.t0 + 2 * tok;
+      }
+      return r;
+    };
+    // This row's loads for a quad: the start of its suffix (visible suffix keys of the row:
+    // [vis_lo, t]) and, with FP8 anchor KV, the quad's K and V scales. Issued for the next
+    // quad after the current one's first tile, used at the next quad.
+    struct RowIn {
+      int vis_lo;
+      float k_sc, v_sc;
+    };
+    auto row_in = [&](const Part& x, int i) {
+      RowIn r{0, 1.0f, 1.0f};
+      if (i < total_items) {
+        const int tt = x.t0 + j * tok + row / G;
+        r.vis_lo = tt < x.tend_j ? __ldg(p.seg + tt) : tt;
+        if (FP8) {
+          r.k_sc = __ldg(p.k_scale + x.ag);
+          r.v_sc = __ldg(p.v_scale + x.ag);
+        }
+      }
+      return r;
+    };
     int item = first;
-    Quad it = item < total_items ? load_quad(p, item) : Quad{};
+    Part it = part_of(item, item < total_items ? load_quad(p, item) : Quad{});
+    RowIn in = row_in(it, item);
     for (; ok && item < total_items; item += stride, ++it_count) {
-      const Quad nxt = item + stride < total_items ? load_quad(p, item + stride) : it;
-      const int nA = it.n_anchor_tiles();
-      const int n = nA + it.n_sfx_tiles();
+      const Quad nxt_raw = item + stride < total_items ? load_quad(p, item + stride) : Quad{};
+      Part nxt{};
+      RowIn nxt_in{0, 1.0f, 1.0f};
+      const int nA = it.nA;
+      const int n = it.n;
       const int g = it.ag % hkv;
       const int t = it.t0 + j * tok + row / G;
-      const bool valid = t < it.tend[j];
-      const int vis_lo = valid ? __ldg(p.seg + t) : t;  // visible suffix keys: [vis_lo, t]
-      const int ws_q = it.wsp[q];
-      const float c_anc = FP8 ? c * __ldg(p.k_scale + it.ag) : c;
-      const float v_sc = FP8 ? __ldg(p.v_scale + it.ag) : 1.0f;
+      const bool valid = t < it.tend_j;
+      const int vis_lo = in.vis_lo;
+      const int ws_q = it.ws_q;
+      const float c_anc = FP8 ? c * in.k_sc : c;
+      const float v_sc = FP8 ? in.v_sc : 1.0f;
       float m_ref = 0.0f, l = 0.0f;
       for (int k = 0; k < n; ++k) {
         if (!(ok = wait_parity(wc, &bars->s_full[q], s_cnt & 1u))) break;
@@ -1321,6 +1412,10 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(p_full_lead);
+        if (k == 0) {  // the next quad's record has arrived by now
+          nxt = part_of(item + stride, nxt_raw);
+          nxt_in = row_in(nxt, item + stride);
+        }
       }
       if (!ok) break;
       // a valid row outside the fast-kernel bounds: the quad's non-empty halves go to the
@@ -1329,10 +1424,9 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
                          (FP8 && it.la > 0 && !(fabsf(v_sc) <= kSpecScaleHigh));
       if (__any_sync(0xFFFFFFFFu, broke && valid) && lane == 0) {
         if (atomicExch(p.redo_flag + item, 1) == 0) {
-          const bool half1 = it.tend[2] > it.t0 + 2 * tok;
-          const int at = atomicAdd(p.redo_count, half1 ? 2 : 1);
+          const int at = atomicAdd(p.redo_count, it.half1 ? 2 : 1);
           p.redo_list[at] = 2 * item;
-          if (half1) p.redo_list[at + 1] = 2 * item + 1;
+          if (it.half1) p.redo_list[at + 1] = 2 * item + 1;
         }
       }
       __syncwarp();
@@ -1369,6 +1463,7 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
       if (valid && p.lse != nullptr)
         p.lse[orow] = (m_ref + __log2f(l)) * 0.69314718055994531f;
       it = nxt;
+      in = nxt_in;
     }
     tc_fence_before();
   }

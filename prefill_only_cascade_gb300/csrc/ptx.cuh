@@ -53,6 +53,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 
+// Non-blocking test of the same condition. try_wait may suspend the thread for a
+// system-dependent time before it returns false, which makes it the right instruction
+// for a wait loop and the wrong one for a poll between other work.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // State shared by the roles of one CTA for bounded waits.
 struct WaitCtl {
   uint64_t timeout_ns;       // how long one wait may block
