@@ -619,6 +619,11 @@ quail_status quail_quantize_kv_fp8_with_scales(int32_t num_anchors,
   q.kv = kv_bf16;
   q.codes = kv_e4m3;
   q.scale = scale;
+  q.err_word = st->err_word;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    q.timeout_ns = g_timeout_ns;
+  }
   const cudaError_t e = quail::launch_quantize_kv_fp8_scaled(
       q, amax, st->num_sms, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QUAIL_OK : QUAIL_ERR_CUDA;

@@ -253,6 +253,12 @@ kv_quantize_kernel(const __grid_constant__ CUtensorMap map, int num_anchors, int
     uint32_t mp = 0;
     for (int r = 0; r < g.rounds; ++r) {
       if (r > 0) issue_round(g, r);  // round 0 was issued ahead
+      // the register vectors were issued first (see pass 2)
+      const int row_base = (r * kChunksPerRound + kSmemChunks) * kRows;
+#pragma unroll
+      for (int i = 0; i < kRegVecs; ++i)
+        if (i < nreg && row_base + reg_row0 + i * reg_row_step < g.rows)
+          mp = absmax_bf16x8(mp, rv[i]);
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int slot = warp + kWarps * k;
@@ -266,11 +272,6 @@ kv_quantize_kernel(const __grid_constant__ CUtensorMap map, int num_anchors, int
           if (row < nrows) mp = absmax_bf16x8(mp, ld_shared_16(base + (row * vpr + col) * 16));
         }
       }
-      const int row_base = (r * kChunksPerRound + kSmemChunks) * kRows;
-#pragma unroll
-      for (int i = 0; i < kRegVecs; ++i)
-        if (i < nreg && row_base + reg_row0 + i * reg_row_step < g.rows)
-          mp = absmax_bf16x8(mp, rv[i]);
     }
     // lanes with the same head: the vph-lane group, repeated every vpr lanes
     for (int off = 1; off < vph; off <<= 1)
@@ -302,6 +303,18 @@ kv_quantize_kernel(const __grid_constant__ CUtensorMap map, int num_anchors, int
     for (int r = 0; r < g.rounds; ++r) {
       if (g.rounds > 1) issue_round(g, r);
       const bool last = r == g.rounds - 1;
+      // the register vectors first, so that the next slab's register loads go out at the
+      // start of this pass rather than its end (their latency was exposed in the next
+      // slab's max pass)
+      const int row_base = (r * kChunksPerRound + kSmemChunks) * kRows;
+#pragma unroll
+      for (int i = 0; i < kRegVecs; ++i) {
+        const int row = row_base + reg_row0 + i * reg_row_step;
+        if (i < nreg && row < g.rows)
+          st_hint_8(reinterpret_cast<uint2*>(codes) + gvec(g, row),
+                    quantize_bf16x8(rv[i], s, rs), pol);
+      }
+      if (last && more) issue_regs(ng, 0);
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int slot = warp + kWarps * k;
@@ -321,15 +334,6 @@ kv_quantize_kernel(const __grid_constant__ CUtensorMap map, int num_anchors, int
         }
         if (last && more) issue_slot(ng, 0, k);
       }
-      const int row_base = (r * kChunksPerRound + kSmemChunks) * kRows;
-#pragma unroll
-      for (int i = 0; i < kRegVecs; ++i) {
-        const int row = row_base + reg_row0 + i * reg_row_step;
-        if (i < nreg && row < g.rows)
-          st_hint_8(reinterpret_cast<uint2*>(codes) + gvec(g, row),
-                    quantize_bf16x8(rv[i], s, rs), pol);
-      }
-      if (last && more) issue_regs(ng, 0);
     }
     if (g.rounds == 0 && more) issue_round(ng, 0);  // this CTA's part was empty
     parity ^= 1;  // the next slab's maxima go to the other buffer (see the barrier note)
@@ -340,17 +344,25 @@ kv_quantize_kernel(const __grid_constant__ CUtensorMap map, int num_anchors, int
   cluster_sync();
 }
 
-// Given amax: one read and one write per element. Each block takes chunks of 2,048
-// consecutive 16-byte vectors (8 per thread, thread t holding vectors t + 256 i, so
-// every load and store instruction of a warp is contiguous; 128 bytes per thread are in
-// flight); a chunk spans few token rows, so the anchor of a row (binary search of the
-// offsets, cached per thread) rarely changes. The scales and their reciprocals of all
-// (anchor, KV head) pairs are formed once per block in shared memory when they fit.
+// Given amax: one read and one write per element, a grid-stride stream of 16-byte loads
+// and 8-byte stores. Each block takes chunks of 2,048 consecutive 16-byte vectors (8 per
+// thread, thread t holding vectors t + 256 i, so every load and store instruction of a
+// warp is contiguous): 128 bytes in flight per thread, 96 KB per SM. (A stream of 16 KB
+// bulk copies through a shared-memory ring, one producer lane per SM, read only 5.1-5.4
+// TB/s on GB300 against 6.6-6.8 for plain loads, and quantised at 38 % of the copy
+// bandwidth.) The scales and their reciprocals of all
+// (anchor, KV head) pairs are formed once per block in shared memory when they fit; a
+// thread's column is the same for all its vectors when a token row's vector count divides
+// 256, and the anchor of a row (binary search of the offsets) and its scale are cached per
+// thread.
 constexpr int kScaledThreads = 256;
 constexpr int kScaledVecs = 8;
+// 3 blocks of 256 threads per SM: the compiler's 80 registers a thread, no spills (a
+// bound of 4 blocks forces 64 registers and spills, and measured slower)
+constexpr int kScaledBlocksPerSm = 3;
 constexpr int kScaleTable = 4096;  // (anchor, KV head) pairs kept in shared memory
 
-__global__ void __launch_bounds__(kScaledThreads) kv_quantize_scaled_kernel(
+__global__ void __launch_bounds__(kScaledThreads, kScaledBlocksPerSm) kv_quantize_scaled_kernel(
     int num_anchors, int64_t T, int hkv, int d, const int32_t* __restrict__ ao,
     const float* __restrict__ amax, const __nv_bfloat16* __restrict__ x,
     uint8_t* __restrict__ codes, float* __restrict__ scale) {
@@ -362,7 +374,7 @@ __global__ void __launch_bounds__(kScaledThreads) kv_quantize_scaled_kernel(
     scale[i] = amax != nullptr ? scale_from_amax(__ldg(amax + i)) : 1.0f;  // no rows: 1
   const int64_t row_vec = static_cast<int64_t>(hkv) * d / 8;  // vectors per token row
   const int64_t total = T * row_vec;
-  if (total == 0) return;
+  if (total == 0 || amax == nullptr) return;
   if (cached) {
     for (int i = threadIdx.x; i < pairs; i += blockDim.x) {
       const float sc = scale_from_amax(__ldg(amax + i));
@@ -373,50 +385,74 @@ __global__ void __launch_bounds__(kScaledThreads) kv_quantize_scaled_kernel(
   const uint64_t pol = l2_policy_evict_first();
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   uint2* cv = reinterpret_cast<uint2*>(codes);
-  int a = 0;
-  int64_t a_lo = 0, a_hi = -1;  // rows of the cached anchor
   const int64_t chunk = static_cast<int64_t>(kScaledThreads) * kScaledVecs;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * chunk;
   const uint32_t rv32 = static_cast<uint32_t>(row_vec);
   const uint32_t vph = static_cast<uint32_t>(d / 8);
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * chunk; base < total;
-       base += static_cast<int64_t>(gridDim.x) * chunk) {
-    // one 64-bit division per chunk; 32-bit arithmetic within it
-    const int64_t base_row = base / row_vec;
-    const uint32_t base_col = static_cast<uint32_t>(base - base_row * row_vec);
+  const bool even = rv32 <= kScaledThreads && kScaledThreads % rv32 == 0;
+  const uint32_t rstep = even ? kScaledThreads / rv32 : 0;
+  int a = 0;
+  int64_t a_lo = 0, a_hi = -1;  // rows of the anchor of the cached scale
+  int64_t pr_cur = -1;
+  float sc = 1.0f, rc = 1.0f;
+  auto anchor_of = [&](int64_t row) {  // anchors are sorted
+    if (row < a_lo || row >= a_hi) {
+      int lo = 0, hi = num_anchors - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(ao + mid) <= row) lo = mid; else hi = mid - 1;
+      }
+      a = lo;
+      a_lo = __ldg(ao + a);
+      a_hi = __ldg(ao + a + 1);
+    }
+  };
+  auto scale_of = [&](int64_t pr) {
+    if (pr != pr_cur) {
+      pr_cur = pr;
+      if (cached) {
+        const float2 t2 = table[pr];
+        sc = t2.x;
+        rc = t2.y;
+      } else {
+        sc = scale_from_amax(__ldg(amax + pr));
+        rc = __frcp_rn(sc);
+      }
+    }
+  };
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * chunk; base < total; base += stride) {
     uint4 v[kScaledVecs];
 #pragma unroll
     for (int i = 0; i < kScaledVecs; ++i) {
       const int64_t e = base + i * kScaledThreads + threadIdx.x;
       if (e < total) v[i] = ld_global_16(xv + e, pol);
     }
+    // one 64-bit division per chunk; 32-bit arithmetic within it
+    const int64_t base_row = base / row_vec;
+    const uint32_t base_col = static_cast<uint32_t>(base - base_row * row_vec);
+    if (even) {
+      const uint32_t o0 = base_col + threadIdx.x;
+      const uint32_t col = o0 % rv32;
+      const int64_t row0 = base_row + o0 / rv32;
 #pragma unroll
-    for (int i = 0; i < kScaledVecs; ++i) {
-      const int64_t e = base + i * kScaledThreads + threadIdx.x;
-      if (e >= total) continue;
-      const uint32_t o = base_col + static_cast<uint32_t>(i * kScaledThreads + threadIdx.x);
-      const uint32_t orow = o / rv32;
-      const int64_t row = base_row + orow;
-      if (row < a_lo || row >= a_hi) {  // the anchor holding this row (anchors are sorted)
-        int lo = 0, hi = num_anchors - 1;
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (__ldg(ao + mid) <= row) lo = mid; else hi = mid - 1;
-        }
-        a = lo;
-        a_lo = __ldg(ao + a);
-        a_hi = __ldg(ao + a + 1);
+      for (int i = 0; i < kScaledVecs; ++i) {
+        const int64_t e = base + i * kScaledThreads + threadIdx.x;
+        if (e >= total) continue;
+        anchor_of(row0 + static_cast<int64_t>(i) * rstep);
+        scale_of(static_cast<int64_t>(a) * hkv + col / vph);
+        st_hint_8(cv + e, quantize_bf16x8(v[i], sc, rc), pol);
       }
-      const int64_t pr = static_cast<int64_t>(a) * hkv + (o - orow * rv32) / vph;
-      float sc, rc;
-      if (cached) {
-        const float2 t = table[pr];
-        sc = t.x;
-        rc = t.y;
-      } else {
-        sc = scale_from_amax(__ldg(amax + pr));
-        rc = __frcp_rn(sc);
+    } else {
+#pragma unroll
+      for (int i = 0; i < kScaledVecs; ++i) {
+        const int64_t e = base + i * kScaledThreads + threadIdx.x;
+        if (e >= total) continue;
+        const uint32_t o = base_col + static_cast<uint32_t>(i * kScaledThreads + threadIdx.x);
+        const uint32_t orow = o / rv32;
+        anchor_of(base_row + orow);
+        scale_of(static_cast<int64_t>(a) * hkv + (o - orow * rv32) / vph);
+        st_hint_8(cv + e, quantize_bf16x8(v[i], sc, rc), pol);
       }
-      st_hint_8(cv + e, quantize_bf16x8(v[i], sc, rc), pol);
     }
   }
 }
@@ -473,14 +509,14 @@ cudaError_t launch_quantize_kv_fp8_scaled(const QuantArgs& q, const float* amax,
       (vecs + chunk - 1) / chunk, (int64_t{q.num_anchors} * q.num_kv_heads + 255) / 256);
   // one wave of resident blocks (grid-stride): no tail of late blocks
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_quantize_scaled_kernel, 256, 0) !=
-          cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_quantize_scaled_kernel,
+                                                    kScaledThreads, 0) != cudaSuccess ||
       per_sm < 1) {
     cudaGetLastError();
     per_sm = 1;
   }
   const int blocks = static_cast<int>(std::min<int64_t>(need, int64_t{num_sms} * per_sm));
-  kv_quantize_scaled_kernel<<<blocks, 256, 0, stream>>>(
+  kv_quantize_scaled_kernel<<<blocks, kScaledThreads, 0, stream>>>(
       q.num_anchors, q.total_tokens, q.num_kv_heads, q.head_dim, q.anchor_offsets, amax,
       static_cast<const __nv_bfloat16*>(q.kv), static_cast<uint8_t*>(q.codes), q.scale);
   return cudaGetLastError();

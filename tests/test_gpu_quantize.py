@@ -46,6 +46,10 @@ CASES = {
     "h1_d64_128_byte_rows": ([5, 300, 12345, 64], 1, 64),
     "h2_d64_two_heads_per_slab": ([7, 2048, 513], 2, 64),
     "h4_d128": ([4096, 777, 1], 4, 128),
+    # KV heads not a power of two: token rows of 48 16-byte vectors do not divide the
+    # given-scale stream's 256 vectors per step (its general index path)
+    "h6_d64_uneven_rows": ([100, 37, 2049], 6, 64),
+    "h3_d128_uneven_rows": ([50, 0, 300], 3, 128),
 }
 
 
