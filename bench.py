@@ -920,12 +920,42 @@ def quantize_oracle_sample(kv, anchor_offsets, codes, scale, anchors=8):
 def measure_bandwidth_kernel(q, args, kind, steps):
     """Per-kernel measurement of the HBM-bound kernels:
     head      restricted head on 2,000,000 rows x 2,560 (bf16)
-    quantize  E4M3 quantisation of the long-anchor workload's anchor K
+    quantize  E4M3 quantisation of the long-anchor workload's anchor K: the line is the
+              given-scale quantiser (the max |x| of every (anchor, KV head) known, as the
+              causal prefill emits it: one read and one write per element); `standalone`
+              is quail_quantize_kv_fp8, which forms the max itself (one read, the slab held
+              on chip across a cluster)
     Returns the kernel's CUDA-event time (L2 flushed between launches), its HBM roofline,
     the oracle baseline and parity."""
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
     pk, src = peaks()
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def timed(run):
+        for _ in range(max(args.warmup, 3)):
+            run()
+        torch.cuda.synchronize()
+        evs = _events(steps)
+        with ClockSampler(0) as clk:
+            for a, b in evs:
+                flush.zero_()  # evict L2 (larger than L2) between timed launches
+                a.record(stream)
+                run()
+                b.record(stream)
+            torch.cuda.synchronize()
+        if q.get_device_error() != q.QUAIL_OK:
+            raise RuntimeError(f"device error during the timed region ({kind})")
+        return statistics.median(a.elapsed_time(b) for a, b in evs), clk.summary()
+
+    def roofline(algo_bytes, ms, kernel, traffic):
+        gbs = algo_bytes / (ms / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": traffic,
+                "peak_source": f"hbm_gbs of {src}", "kernel": kernel, "kernel_ms": round(ms, 4),
+                "algorithmic_bytes_per_launch": algo_bytes}
+
+    sub = {}
     if kind == "head":
         cfg = workloads.HEAD_CONFIGS["head"]
         n = args.head_rows or cfg.num_rows
@@ -936,8 +966,10 @@ def measure_bandwidth_kernel(q, args, kind, steps):
                                         stream=stream)
         algo_bytes = n * (cfg.hidden * 2 + 8 * 4 + 4) + cfg.hidden * 2 * 9
         units, unit = n, "rows/s"
-        kernel = "restricted_head_kernel"
         config = {"workload": "head", "rows": n, "hidden": cfg.hidden}
+        ms, clocks = timed(run)
+        roof = roofline(algo_bytes, ms, "restricted_head_kernel",
+                        traffic_from_profile("head.cu", "restricted_head.md"))
     else:
         cfg = workloads.ATTN_CONFIGS["fp8_long"]
         lay = workloads.make_layout(cfg)
@@ -946,51 +978,52 @@ def measure_bandwidth_kernel(q, args, kind, steps):
         codes = torch.empty(kv.shape, dtype=torch.uint8, device=dev)
         scale = torch.empty(cfg.num_anchors, cfg.num_kv_heads, dtype=torch.float32, device=dev)
         ao = torch.from_numpy(lay.anchor_offsets.copy()).to(dev)
-        run = lambda: q.quantize_kv_fp8(kv, ao, codes, scale, stream=stream)
+        # input of the given-scale call (in the pipeline the causal prefill's k_amax): max
+        # |x| per (anchor, KV head), every anchor of this workload having the same length
+        la = cfg.anchor_len[0]
+        amax = kv.view(cfg.num_anchors, la, cfg.num_kv_heads, cfg.head_dim).abs().amax(
+            dim=(1, 3)).float().contiguous()
         algo_bytes = kv.numel() * 3 + scale.numel() * 4
         units, unit = kv.numel(), "elements/s"
-        kernel = "kv_quantize_kernel"
         config = {"workload": "quantize", "anchors": cfg.num_anchors,
                   "anchor_len": cfg.anchor_len[0], "kv_heads": cfg.num_kv_heads,
-                  "head_dim": cfg.head_dim}
-    for _ in range(max(args.warmup, 3)):
-        run()
-    torch.cuda.synchronize()
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    evs = _events(steps)
-    with ClockSampler(0) as clk:
-        for a, b in evs:
-            flush.zero_()  # evict L2 (larger than L2) between timed launches
-            a.record(stream)
-            run()
-            b.record(stream)
-        torch.cuda.synchronize()
+                  "head_dim": cfg.head_dim, "scales": "given (max |x| per anchor and KV head)"}
+        codes_sa = torch.empty_like(codes)
+        scale_sa = torch.empty_like(scale)
+        ms_sa, clocks_sa = timed(lambda: q.quantize_kv_fp8(kv, ao, codes_sa, scale_sa,
+                                                           stream=stream))
+        sub["standalone"] = {
+            "kernel_ms": round(ms_sa, 4),
+            "roofline": roofline(algo_bytes, ms_sa, "kv_quantize_kernel (forms the max itself)",
+                                 traffic_from_profile("quantize.cu", "quantize_fp8_long.md")),
+            "clocks": clocks_sa}
+        ms, clocks = timed(lambda: q.quantize_kv_fp8_with_scales(kv, ao, amax, codes, scale,
+                                                                 stream=stream))
+        roof = roofline(algo_bytes, ms, "kv_quantize_scaled_kernel (given scales)",
+                        traffic_from_profile("quantize.cu", "quantize_scaled_fp8_long.md"))
+        sub["standalone"]["same_codes_as_given_scale"] = bool(
+            torch.equal(codes, codes_sa) and torch.equal(scale, scale_sa))
     del flush
-    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
-    gbs = algo_bytes / (ms / 1e3) / 1e9
     cpu = parity = None
     if not args.no_cpu_baseline:
         if kind == "head":
             cpu, parity = head_oracle_sample(x["h"], x["gamma"], x["w8"], cfg.eps, logits, am)
         else:
             cpu, parity = quantize_oracle_sample(kv, lay.anchor_offsets, codes, scale)
+            sub["standalone"]["parity"] = quantize_oracle_sample(
+                kv, lay.anchor_offsets, codes_sa, scale_sa, anchors=1)[1]
     config["l2"] = "flushed between launches"
     res = {"metric": f"{kind} kernel throughput", "value": units / (ms / 1e3), "unit": unit,
            "steps": steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
-           "config": config,
-           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
-                        "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
-                        "traffic": (traffic_from_profile("quantize.cu", "quantize_fp8_long.md")
-                                    if kind == "quantize" else
-                                    traffic_from_profile("head.cu", "restricted_head.md")),
-                        "peak_source": f"hbm_gbs of {src}", "kernel": kernel,
-                        "kernel_ms": round(ms, 4), "algorithmic_bytes_per_launch": algo_bytes},
+           "config": config, "roofline": roof,
            "cpu_baseline": cpu, "parity": parity, "gpu_launches": steps,
-           "clocks": clk.summary()}
+           "clocks": clocks}
+    if sub:
+        res["sub"] = sub
     if kind == "head":
         del x, logits, am
     else:
-        del kv, codes, scale
+        del kv, codes, scale, codes_sa, scale_sa, amax
     torch.cuda.empty_cache()
     return res
 
