@@ -1968,8 +1968,9 @@ void set_cta_pairs(int mode) { g_cta_pairs.store(mode); }
 
 cudaError_t launch_cascade(const CascadeParams& params, const CascadeMaps& maps, int head_dim,
                            bool fp8, int num_sms, cudaStream_t stream) {
-  // The CTA-pair kernel takes d = 128 calls with both parts fused and no K/V amax (the
-  // fault-injection switch exercises the single-CTA kernel's timeout path). Automatic
+  // The CTA-pair kernel takes d = 128 calls with both parts fused and no K/V amax (with
+  // the fault-injection switch on, only when forced: then its own timeout path runs, else
+  // the single-CTA kernel's). Automatic
   // choice: a pair tile's suffix window spans two query tiles and is loaded as 128-key
   // tiles, while the single-CTA kernel loads a window of at most 64 keys as one 64-key
   // tile; when every query tile's window fits in 64 keys (tokens per tile + the longest
@@ -1978,7 +1979,8 @@ cudaError_t launch_cascade(const CascadeParams& params, const CascadeMaps& maps,
   CascadeParams p = params;
   const int mode = g_cta_pairs.load();
   bool pairs = mode != QUAIL_CTA_PAIRS_OFF && head_dim == 128 && p.mode == kFused &&
-               p.k_amax == nullptr && p.inject_skip_first_kv == 0 && num_sms >= 2;
+               p.k_amax == nullptr && num_sms >= 2 &&
+               (p.inject_skip_first_kv == 0 || mode == QUAIL_CTA_PAIRS_ALWAYS);
   if (mode == QUAIL_CTA_PAIRS_AUTO && p.tok_per_tile + p.max_suffix_len - 1 <= 64) pairs = false;
   p.tiles_per_item = pairs ? 4 : 2;
   cudaError_t e = cudaMemsetAsync(p.flag, 0, sizeof(int32_t), stream);
