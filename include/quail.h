@@ -343,8 +343,8 @@ quail_status quail_restricted_head(int64_t n_rows, int32_t hidden, float eps, co
  *   nearest even with saturation at +-448 (sign kept).
  *   kv_bf16 [T_A, Hkv, d] bf16 in; kv_e4m3 [T_A, Hkv, d] codes out; scale [A, Hkv] fp32
  *   out. d in {64, 128}, Hkv * d <= 4096. One kernel on `stream` (clusters of 8 CTAs
- *   holding each (anchor, KV head) slab in shared memory: one read of kv_bf16 for
- *   anchors up to 6,144 tokens at d = 128, two reads above). Offsets are clamped into
+ *   holding each (anchor, KV head) slab on chip: one read of kv_bf16 for anchors up to
+ *   4,096 tokens at 256-byte token rows per slab, two reads above). Offsets are clamped into
  *   [0, T_A] on the device, so inconsistent ones cannot address outside the tensors.
  */
 quail_status quail_quantize_kv_fp8(int32_t num_anchors, const int32_t* anchor_offsets,

@@ -1,9 +1,10 @@
 """GPU parity of the E4M3 quantisers against the oracle, bit for bit (codes and scales).
 
-quail_quantize_kv_fp8 keeps each (anchor, KV head) slab in an 8-CTA cluster's shared
-memory up to 24 chunks of 32 rows per CTA (6,144 tokens) and reads longer anchors twice;
+quail_quantize_kv_fp8 keeps each (anchor, KV head) slab on an 8-CTA cluster's chips up to
+16 chunks of 32 rows per CTA (4,096 tokens) and reads longer anchors twice, in rounds;
 the cases cover empty anchors, chunk and part edges (31, 32, 33, 255, 256, 257 rows),
-both sides of the on-chip limit, 128- and 256-byte rows (one or two heads per slab).
+both sides of the on-chip limit, 128- and 256-byte rows (one or two heads per slab), and
+KV head counts that are not powers of two.
 quail_quantize_kv_fp8_with_scales takes the amax; quail_causal_prefill_attn can emit it
 (k_amax / v_amax) from the K/V tiles it loads, which must equal max |x| exactly and leave
 the attention output unchanged."""
