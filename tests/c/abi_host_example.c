@@ -80,5 +80,11 @@ int main(void) {
   CHECK(quail_kv_plan(3, size, 5, acc, 8, QUAIL_KV_LRU, hit, &st) == QUAIL_OK &&
             st.regret_tokens > 0,
         "lru regrets");
+  /* kernel choice for head_dim 128: the three modes, anything else rejected */
+  CHECK(quail_set_cta_pairs(QUAIL_CTA_PAIRS_OFF) == QUAIL_OK &&
+            quail_set_cta_pairs(QUAIL_CTA_PAIRS_ALWAYS) == QUAIL_OK &&
+            quail_set_cta_pairs(7) == QUAIL_ERR_INVALID_ARG &&
+            quail_set_cta_pairs(QUAIL_CTA_PAIRS_AUTO) == QUAIL_OK,
+        "cta pair modes");
   return failures == 0 ? 0 : 1;
 }
