@@ -24,4 +24,4 @@ def test_plain_c_program_uses_the_abi(tmp_path):
     assert build.returncode == 0, build.stderr
     run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert run.returncode == 0, run.stdout + run.stderr
-    assert "FAILED" not in run.stdout and run.stdout.count("ok ") == 13
+    assert "FAILED" not in run.stdout and run.stdout.count("ok ") == 14
