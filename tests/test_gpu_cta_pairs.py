@@ -139,3 +139,29 @@ def test_full_size_both_kernels_sampled_rows(name):
     del t, out1, out2, lse1, lse2, res
     torch.cuda.empty_cache()
 
+
+
+@pytest.mark.parametrize("seed", range(32))
+def test_random_layouts_both_kernels_every_element(seed):
+    # seeded random layouts: 1-6 anchors of 0-700 tokens, 0-12 suffixes each of 1-150
+    # tokens, G in {1, 2, 4, 8, 16}; both kernels forced, every element against the oracle
+    import prefill_only_cascade_gb300 as q
+    rng = np.random.default_rng(1000 + seed)
+    na = int(rng.integers(1, 7))
+    anchors = [int(x) for x in rng.integers(0, 701, size=na)]
+    counts = [int(x) for x in rng.integers(0, 13, size=na)]
+    if sum(counts) == 0:
+        counts[0] = 1
+    lens = [int(x) for x in rng.integers(1, 151, size=sum(counts))]
+    g = int(rng.choice([1, 2, 4, 8, 16]))
+    hkv = int(rng.choice([1, 2]))
+    heads = (g * hkv, hkv, 128)
+    lay = workloads.layout_from_lengths(anchors, counts, lens)
+    t = _inputs(lay, heads, seed=seed)
+    try:
+        for mode in (q.CTA_PAIRS_ALWAYS, q.CTA_PAIRS_OFF):
+            q.set_cta_pairs(mode)
+            out, lse = run_cascade(heads, lay, t)
+            print(seed, mode, heads, anchors, counts, check_full(heads, lay, t, out, lse))
+    finally:
+        q.set_cta_pairs(q.CTA_PAIRS_AUTO)
