@@ -21,10 +21,14 @@
 //                                        suffix holding token t
 //   3. cascade_schedule_kernel  (1 CTA)  anchor checks; anchors ordered by decreasing
 //                                        anchor-tile count; prefix sum of work items
-//   4. cascade_items_kernel     (grid)   one 32-byte record per work item
+//   4. cascade_items_kernel     (grid)   one record per work item (a quad of four query
+//                                        tiles for the CTA-pair kernel)
 //   5. anchor_e4m3_to_bf16_kernel (grid, FP8 anchor KV only) stages the anchor codes as
 //                                        bf16 in the workspace
-//   6. cascade_attn_kernel      (persistent, one CTA per SM), fast then exact instance
+//   6. the fast kernel - cascade_attn_kernel (persistent, one CTA per SM) or, for d = 128
+//      with suffix windows beyond 64 keys, cascade_pair_kernel (persistent clusters of two
+//      CTAs, 256-row tcgen05 MMAs over an SM pair) - then cascade_attn_kernel's exact
+//      instance over the items the fast kernel listed
 //
 // Per CTA of the attention kernel:
 //   warp 8      TMA producer: Q tiles, then a ring of K / V tiles (128 keys each)
