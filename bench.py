@@ -1117,9 +1117,10 @@ def run_prefill(args):
             "roofline": {"bound": "tensor", "achieved": round(tflops, 2),
                          "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(tflops / pk["bf16_tflops"], 4),
-                         "traffic": traffic_from_profile("cascade.cu", "cascade_attn_prefill.md"),
+                         "traffic": (None if pair_kernel(lay, hq, hkv, d) else
+                                     traffic_from_profile("cascade.cu", "cascade_attn_prefill.md")),
                          "peak_source": f"bf16_tflops (burst) of {src}",
-                         "kernel": "cascade_attn_kernel (anchors of length 0), one call",
+                         "kernel": (("cascade_pair_kernel (CTA pairs)" if pair_kernel(lay, hq, hkv, d) else "cascade_attn_kernel") + " with anchors of length 0, one call"),
                          "algorithmic_flops_per_launch": flops},
             "gpu_launches": 6 * args.steps, "clocks": clk.summary()}
     if not args.no_cpu_baseline:
