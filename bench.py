@@ -160,20 +160,38 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def code_digest(path: str) -> str:
+    """sha256 of a source file's code: `//` comments, trailing blanks and empty lines
+    removed, so that a comment edit does not disown a profile taken on the same code."""
+    lines = []
+    for line in open(path, encoding="utf-8"):
+        i = line.find("//")
+        if i >= 0:
+            line = line[:i]
+        line = line.rstrip()
+        if line:
+            lines.append(line)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
+
+
 def traffic_from_profile(kernel_file: str, profile_md: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
-    kernel source (the summary records the source's sha256)."""
+    kernel code (the summary records `kernel_code_sha256`, the code_digest of the source,
+    or an older whole-file `kernel_source_sha256`)."""
     path = os.path.join(ROOT, "profiles", profile_md)
     src = os.path.join(ROOT, "prefill_only_cascade_gb300", "csrc", kernel_file)
     if not (os.path.exists(path) and os.path.exists(src)):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
     vals = {}
     for line in open(path):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
-    if vals.get("kernel_source_sha256") != sha:
+    if "kernel_code_sha256" in vals:
+        ok = vals["kernel_code_sha256"] == code_digest(src)
+    else:
+        ok = vals.get("kernel_source_sha256") == hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if not ok:
         return None
     try:
         return float(vals["traffic_bytes_per_launch"])

@@ -950,15 +950,16 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
 // loads and holds half of it: keys 64 r .. 64 r + 63 of the K tile (the N half of the B
 // operand of S = Q K^T) and d columns 64 r .. 64 r + 63 of the V tile (the N half of the B
 // operand of O += P V). Per SM and K16 step, S then reads 4 KB (its own query rows) + 2 KB
-// (its K half) of shared memory instead of 8 KB, and a quad has half the item boundaries
-// per query tile of a pair item.
+// (its K half) of shared memory instead of 8 KB, and each SM loads half of every K/V tile.
 // Synchronisation: rank 0's MMA warp issues every MMA for both CTAs, and its commits
 // arrive on the barrier of the same name in both CTAs (slot free, S ready, query tile
 // free, O done). Both CTAs' TMA loads complete on rank 0's full barriers, for which rank 0
 // expects both halves' bytes; both CTAs' softmax warps arrive on rank 0's P-ready barrier
 // (9 arrivals: 2 x 4 softmax warps + rank 0's fill checker). Rank 1's MMA warp takes part
-// only in the TMEM allocation. Suffix tiles always use N = 128 (a 64-key tile would split
-// 32 / 32 between the CTAs, not as the 64-row K halves are loaded).
+// only in the TMEM allocation and release. Barrier waits and remote arrivals keep the
+// default CTA-scope semantics (no data moves through generic memory between the CTAs).
+// Suffix tiles always use N = 128 (a 64-key tile would split 32 / 32 between the CTAs, not
+// as the 64-row K halves are loaded).
 struct PairCfg {
   static constexpr int kKB = 2;                          // 128-byte column blocks (d = 128)
   static constexpr int kBlockBytes = 128 * 128;          // 128 rows x 128 bytes
