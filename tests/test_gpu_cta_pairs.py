@@ -165,3 +165,20 @@ def test_random_layouts_both_kernels_every_element(seed):
             print(seed, mode, heads, anchors, counts, check_full(heads, lay, t, out, lse))
     finally:
         q.set_cta_pairs(q.CTA_PAIRS_AUTO)
+
+
+@pytest.mark.parametrize("lens", [(1, 30), (40, 200)])
+def test_pair_kernel_redo_lists_quad_halves(lens, pairs_always):
+    # anchor 1's keys past its first tile x 40: its quads leave the fast bounds and hand
+    # their non-empty halves (two-tile items) to the exact kernel; the other anchors stay
+    # fast. Count: 2 KV heads x ceil(tokens / 64) halves (G = 4: 32 tokens a query tile).
+    from test_gpu_redo import _case
+    lay, t = _case([200, 300, 150], [3, 3, 3], lens, (8, 2, 128), 12)
+    ao = lay.anchor_offsets
+    lo, hi = int(ao[1]) + 128, int(ao[2])
+    t["k_anc"][lo:hi] = (t["k_anc"][lo:hi].float() * 40).to(torch.bfloat16)
+    out, lse, ws = run_cascade((8, 2, 128), lay, t, keep_ws=True)
+    so, asp = lay.suffix_offsets, lay.anchor_suffix_ptr
+    ntok = int(so[asp[2]] - so[asp[1]])
+    assert redo_count(ws) == 2 * ((ntok + 63) // 64)
+    print(lens, check_full((8, 2, 128), lay, t, out, lse))
