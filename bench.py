@@ -529,6 +529,8 @@ def measure_attention(q, cfg, layout, dev, args, *, steps, e2e=False, cpu_budget
     hcfg = workloads.HEAD_CONFIGS["join_last_token"]
     hx = workloads.make_head_inputs(hcfg, dev, num_rows=layout.total_suffix_tokens)
     last = torch.from_numpy((layout.suffix_offsets[1:] - 1).astype(np.int32)).to(dev)
+    # the end-to-end leg's pinned host inputs, made before anything else churns host memory
+    e2e_host = e2e_host_inputs(t, hx["h"], last, k_scale, v_scale) if e2e else None
     S = layout.num_suffixes
     logits = torch.empty(S, 8, dtype=torch.float32, device=dev)
     am = torch.empty(S, dtype=torch.int32, device=dev)
@@ -615,6 +617,13 @@ def measure_attention(q, cfg, layout, dev, args, *, steps, e2e=False, cpu_budget
            "gpu_launches": (7 if kv_fp8 and layout.total_anchor_tokens > 0 else 6) * steps,
            "clocks": clk.summary()}
 
+    if e2e:
+        # right after the device-timed region, while the box is in the same state (after
+        # seconds of host-only work the copies ran ~10 % slower)
+        res["e2e"] = run_e2e_chunked(q, cfg, layout, t, hx["h"], last, k_scale, v_scale, dev,
+                                     stream, world, steps=max(3, min(steps, 6)),
+                                     host=e2e_host)
+        del e2e_host
     parity_refs = {}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         def host_cases(ids):
@@ -638,9 +647,6 @@ def measure_attention(q, cfg, layout, dev, args, *, steps, e2e=False, cpu_budget
         res["fused_vs_two_pass"] = compare_two_pass(
             q, desc, t, out, lse, k_scale, v_scale, attn_ms, max(3, min(steps, 5)), stream,
             parity_refs)
-    if e2e:
-        res["e2e"] = run_e2e_chunked(q, cfg, layout, t, hx["h"], last, k_scale, v_scale, dev,
-                                     stream, world, steps=max(3, min(steps, 6)))
     del t, t_bf16, ws, out, lse, hx
     torch.cuda.empty_cache()
     return res
@@ -678,8 +684,32 @@ def _chunks(layout, n):
     return [(cuts[i], cuts[i + 1]) for i in range(len(cuts) - 1)]
 
 
+def e2e_host_inputs(t, h_all, last, k_scale, v_scale):
+    """The step's inputs in pinned host memory (queries, anchor and suffix K/V, the hidden
+    states of the last tokens, FP8 scales), as a caller of the end-to-end path holds them.
+    Made once, early in the process: pinned buffers made after much host allocation churn
+    (a second or third 57 GB set in one process) fed the host-to-device copies at ~155
+    instead of ~210 GB/s on GB300."""
+    def pinned_like(x):
+        return torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    names = ["q_suf", "k_anc", "v_anc", "k_suf", "v_suf"]
+    host = {k: pinned_like(t[k]) for k in names}
+    for k in names:
+        host[k].copy_(t[k])
+    h_last = h_all.index_select(0, last.long())
+    host["h"] = pinned_like(h_last)
+    host["h"].copy_(h_last)
+    del h_last
+    if k_scale is not None:
+        host["k_scale"] = pinned_like(k_scale)
+        host["v_scale"] = pinned_like(v_scale)
+        host["k_scale"].copy_(k_scale)
+        host["v_scale"].copy_(v_scale)
+    return host
+
+
 def run_e2e_chunked(q, cfg, layout, t, h_all, last, k_scale, v_scale, dev, stream, world,
-                    steps, n_chunks=8):
+                    steps, n_chunks=8, host=None):
     """Same metric through the C ABI with host buffers. Every step copies all of its inputs
     from pinned host memory (queries, anchor and suffix K/V, offsets, the hidden states of
     the last tokens) and reads the step's result (logits and argmax) back. The batch goes
@@ -692,21 +722,12 @@ def run_e2e_chunked(q, cfg, layout, t, h_all, last, k_scale, v_scale, dev, strea
     so = layout.suffix_offsets.astype(np.int64)
     chunks = _chunks(layout, min(n_chunks, layout.num_anchors))
     # host copies of every input (pinned), written from the device-resident tensors
-    def pinned_like(x):
-        return torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-    names = ["q_suf", "k_anc", "v_anc", "k_suf", "v_suf"]
-    host = {k: pinned_like(t[k]) for k in names}
-    for k in names:
-        host[k].copy_(t[k])
-    h_last = h_all.index_select(0, last.long())
-    host["h"] = pinned_like(h_last)
-    host["h"].copy_(h_last)
-    del h_last
+    if host is None:
+        host = e2e_host_inputs(t, h_all, last, k_scale, v_scale)
+    host = dict(host)
     sc = None
-    if k_scale is not None:
-        sc = {"k": pinned_like(k_scale), "v": pinned_like(v_scale)}
-        sc["k"].copy_(k_scale)
-        sc["v"].copy_(v_scale)
+    if "k_scale" in host:
+        sc = {"k": host.pop("k_scale"), "v": host.pop("v_scale")}
     plan = []
     for a0, a1 in chunks:
         s0, s1 = int(asp[a0]), int(asp[a1])
