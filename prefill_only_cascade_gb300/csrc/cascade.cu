@@ -1908,6 +1908,11 @@ static int pair_clusters(int num_sms, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   std::atomic<int>* slot = dev >= 0 && dev < 64 ? &cache[dev] : nullptr;
   if (slot != nullptr && slot->load() > 0) return slot->load();
+  if (cudaFuncSetAttribute(cascade_pair_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           PairCfg::kSmemBytes) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
   int clusters = 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(num_sms / 2 * 2), 1, 1);
@@ -1987,6 +1992,9 @@ cudaError_t launch_cascade(const CascadeParams& params, const CascadeMaps& maps,
                p.k_amax == nullptr && num_sms >= 2 &&
                (p.inject_skip_first_kv == 0 || mode == QUAIL_CTA_PAIRS_ALWAYS);
   if (mode == QUAIL_CTA_PAIRS_AUTO && p.tok_per_tile + p.max_suffix_len - 1 <= 64) pairs = false;
+  // no resident pair of SMs (e.g. a partition of the GPU): the single-CTA kernel
+  if (pairs && (fp8 ? pair_clusters<true>(num_sms, stream) : pair_clusters<false>(num_sms, stream)) <= 0)
+    pairs = false;
   p.tiles_per_item = pairs ? 4 : 2;
   cudaError_t e = cudaMemsetAsync(p.flag, 0, sizeof(int32_t), stream);
   if (e != cudaSuccess) return e;
