@@ -83,10 +83,11 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 3-D bf16 tensor map over [tokens, heads, d] (innermost d), 128-byte swizzle, box
-// (64 elements of d, box_heads, box_rows); out-of-range rows read as zero.
+// 3-D tensor map over [tokens, heads, d] (innermost d), box (box_inner elements of d,
+// box_heads, box_rows), 128-byte swizzle unless given; out-of-range rows read as zero.
 bool encode_3d(CUtensorMap* m, const void* base, int64_t tokens, int heads, int d,
-               int box_heads, int box_rows, CUtensorMapDataType dt, int elem_bytes, int box_inner) {
+               int box_heads, int box_rows, CUtensorMapDataType dt, int elem_bytes, int box_inner,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
                               static_cast<cuuint64_t>(tokens)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elem_bytes,
@@ -96,7 +97,7 @@ bool encode_3d(CUtensorMap* m, const void* base, int64_t tokens, int heads, int 
                              static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[3] = {1, 1, 1};
   return g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -274,6 +275,10 @@ quail_status prepare_cascade(const quail_cascade_desc* desc, const void* q_suf, 
     maps.v_anc = maps.v_suf;
     maps.k_anc64 = maps.k_suf64;
   }
+  // the output, for the epilogue's TMA stores: one warp's 32 rows (32 / G tokens x G heads)
+  // by 32 columns of d, 64 bytes a row (64-byte swizzle)
+  ok = ok && encode_3d(&maps.out, out, d.total_suffix_tokens, d.num_q_heads, D, group, 32 / group,
+                       bf, 2, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   if (!ok) return QUAIL_ERR_CUDA;
 
   quail::CascadeParams& p = *pp;

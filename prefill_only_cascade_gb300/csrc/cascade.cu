@@ -73,6 +73,7 @@ constexpr int kThreads = 384;             // three warpgroups
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 constexpr int kWarpFillCheck = 10;
+constexpr int kWarpQLoad = 11;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: O is rescaled only past 2^8
 // Fast kernel bounds (P = 2^(s c) with no max subtracted); outside them the item goes to
 // the exact kernel. The row sum l = sum P must lie in [2^-64, 2^32]: every P <= l <= 2^32
@@ -87,6 +88,10 @@ constexpr float kSpecScaleHigh = 1.8446744073709552e19f;  // 2^64
 constexpr int kSortBins = 1024;
 constexpr uint32_t kTmemCols = 512;
 
+// Shared-memory staging of the epilogue: two 2 KB buffers per softmax warp.
+constexpr int kStageWarpBytes = 2 * 2048;
+constexpr int kSmemStage = 8 * kStageWarpBytes;
+
 template <int D>
 struct Cfg {
   static constexpr int kKB = D / 64;                   // 128-byte column blocks per row
@@ -95,7 +100,8 @@ struct Cfg {
   static constexpr int kStages = (D == 128) ? 2 : 4;
   static constexpr int kSmemQ = 2 * kTileBytes;
   static constexpr int kSmemKV = kStages * 2 * kTileBytes;
-  static constexpr int kSmemBytes = kSmemQ + kSmemKV + 1024 + 1024;
+  // queries, K/V ring, barriers (1 KB), epilogue staging, alignment slack (1 KB)
+  static constexpr int kSmemBytes = kSmemQ + kSmemKV + 1024 + kSmemStage + 1024;
   static constexpr int kRegsSoftmax = (D == 128) ? 176 : 184;
   static constexpr int kRegsOther = (D == 128) ? 152 : 136;
   static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= 384 * 168, "register split");
@@ -208,6 +214,54 @@ __device__ __forceinline__ void st_global_v8(void* p, const uint32_t* v) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
                "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
+}
+
+// Epilogue of one warp whose 32 rows are all valid output rows: O / l as bf16 through
+// shared memory and TMA tensor stores. The warp's TMEM lanes are 32 / G consecutive
+// tokens x G heads, which is one box (32 columns of d, G heads, 32 / G tokens) of the
+// output map. Each 32-column chunk (64 bytes a row, 2 KB the warp) goes to one of two
+// buffers with the 64-byte swizzle (16-byte chunk c of row r at c ^ ((r >> 1) & 3), so
+// each st.shared of the warp takes the minimum four wavefronts) and leaves by one TMA
+// store; a buffer is rewritten only once the store issued from it before has read it.
+// The per-thread 32-byte row stores this replaces touch 32 cache lines per instruction.
+template <int D>
+__device__ __forceinline__ void store_rows_tma(const CUtensorMap* map, uint32_t t_o, uint64_t il,
+                                               uint32_t stage, int lane, int head0, int tok0,
+                                               uint64_t policy) {
+  const uint32_t row_addr = stage + static_cast<uint32_t>(lane) * 64u;
+  const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll
+  for (int ch2 = 0; ch2 < D / 64; ++ch2) {
+    uint32_t r[2][32];
+    tmem_ld32(t_o + ch2 * 64, r[0]);
+    tmem_ld32(t_o + ch2 * 64 + 32, r[1]);
+    tmem_wait_ld_dep(r[0]);
+    reg_dep(r[1]);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        float lo, hi;
+        f2_split(f2_mul(f2(__uint_as_float(r[h][2 * e]), __uint_as_float(r[h][2 * e + 1])), il),
+                 lo, hi);
+        pk[e] = pack_bf16(lo, hi);
+      }
+      if (lane == 0) bulk_wait_group_read<1>();
+      __syncwarp();
+      const uint32_t buf = static_cast<uint32_t>(h) * 2048u;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        st_shared_v4(row_addr + buf + 16u * (static_cast<uint32_t>(c) ^ sw), pk[4 * c],
+                     pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d_hint(map, stage + buf, ch2 * 64 + h * 32, head0, tok0, policy);
+        bulk_commit_group();
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------------
@@ -430,7 +484,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       }
       const uint64_t keep = l2_policy_evict_last(), stream_pol = l2_policy_evict_first();
       uint32_t kv_seq = 0, it_count = 0;
-      uint32_t q_arm[2] = {0, 0}, k_arm[4] = {0, 0, 0, 0}, v_arm[4] = {0, 0, 0, 0};
+      uint32_t k_arm[4] = {0, 0, 0, 0}, v_arm[4] = {0, 0, 0, 0};
       bool skip_pending = p.inject_skip_first_kv != 0;
       bool ok = true;
       // AMAX: per-row max |x| of the K (kv = 0) or V (kv = 1) tile in `slot`, over the rows
@@ -548,21 +602,6 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
             }
             __syncwarp();
           }
-          if (pos == 0) {
-            for (int q = 0; q < 2 && ok; ++q) {
-              if (!(ok = wait_parity_warp(wc, &bars->q_empty[q], (it_count & 1u) ^ 1u))) break;
-              ++q_arm[q];
-              if (leader) {
-                mbar_arrive_expect_tx(&bars->q_full[q], C::kTileBytes);
-                for (int kb = 0; kb < C::kKB; ++kb)
-                  tma_load_3d_hint(&maps.q, &bars->q_full[q],
-                                   sQ + q * C::kTileBytes + kb * C::kBlockBytes, kb * 64, g * G,
-                                   it.t0 + q * tok, stream_pol);
-              }
-              __syncwarp();
-            }
-            if (!ok) break;
-          }
           service();
           if (!(ok = wait_parity_warp(wc, &bars->v_empty[slot], ph ^ 1u))) break;
           if (AMAX) {
@@ -604,8 +643,6 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       }
       // Let every load that was issued land before the CTA can exit.
       const uint64_t dl = global_timer_ns() + 100000000ull;
-      for (int q = 0; q < 2; ++q)
-        if (q_arm[q]) drain_wait(&bars->q_full[q], (q_arm[q] - 1) & 1u, dl);
       for (int s = 0; s < C::kStages; ++s) {
         bool landed = true;
         if (k_arm[s]) landed &= drain_wait(&bars->k_full[s], (k_arm[s] - 1) & 1u, dl);
@@ -617,6 +654,37 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
         }
       }
     }
+   } else if (warp == kWarpQLoad) {
+    // ------------------------------------------------ query loader
+    // Each item's two query tiles load as soon as their buffers are free (the commit after
+    // the previous item's last S of that tile), apart from the K/V ring: a producer that
+    // issued them in ring order held them back until a K/V slot freed, and the next item's
+    // first S then waited for the query tile at every item boundary.
+    const bool leader = elect_one();
+    const uint64_t stream_pol = l2_policy_evict_first();
+    uint32_t it_count = 0, q_arm[2] = {0, 0};
+    bool ok = true;
+    int item = blockIdx.x;
+    Item it = item < total_items ? load_item<EXACT>(p, item_id(item)) : Item{};
+    for (; ok && item < total_items; item += stride, ++it_count) {
+      const Item nxt = item + stride < total_items ? load_item<EXACT>(p, item_id(item + stride)) : it;
+      const int g = it.ag % hkv;
+      for (int q = 0; q < 2 && ok; ++q) {
+        if (!(ok = wait_parity_warp(wc, &bars->q_empty[q], (it_count & 1u) ^ 1u))) break;
+        ++q_arm[q];
+        if (leader) {
+          mbar_arrive_expect_tx(&bars->q_full[q], C::kTileBytes);
+          for (int kb = 0; kb < C::kKB; ++kb)
+            tma_load_3d_hint(&maps.q, &bars->q_full[q], sQ + q * C::kTileBytes + kb * C::kBlockBytes,
+                             kb * 64, g * G, it.t0 + q * tok, stream_pol);
+        }
+        __syncwarp();
+      }
+      it = nxt;
+    }
+    const uint64_t dl = global_timer_ns() + 100000000ull;
+    for (int q = 0; q < 2; ++q)
+      if (q_arm[q]) drain_wait(&bars->q_full[q], (q_arm[q] - 1) & 1u, dl);
    } else if (warp == kWarpFillCheck) {
     // ------------------------------------------------ fill checker
     // For every group {PV(q,k), S(q,k+1)}: wait until the V(q,k) and K(q,k+1) fills it
@@ -784,6 +852,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + lane_base + 256u * q;
     const uint32_t t_o = t_s + 128u;
+    const uint32_t stage = smem_u32(smem + C::kSmemQ + C::kSmemKV + 1024) + warp * kStageWarpBytes;
+    const uint64_t out_pol = l2_policy_evict_first();
     uint32_t s_cnt = 0, it_count = 0;
     bool ok = true;
     const float c = p.scale_log2;
@@ -873,8 +943,13 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       const uint64_t wo = f2(w_own, w_own), wp = f2(w_part, w_part);
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + orow * D;
       float* out32 = p.mode == kAnchorPass ? p.o_part + orow * D : nullptr;
+      if (p.mode == kFused && __all_sync(0xFFFFFFFFu, valid)) {
+        store_rows_tma<D>(&maps.out, t_o, wo, stage, lane, g * G,
+                          it.t0 + q * tok + (warp & 3) * (32 / G), out_pol);
+      } else {
       // Two 32-column chunks of O per TMEM wait; each thread writes its row with 32-byte
-      // stores (one full sector each).
+      // stores (one full sector each): the rows of a partly valid warp and the
+      // two-pass variant's outputs.
 #pragma unroll
       for (int ch2 = 0; ch2 < D / 64; ++ch2) {
         uint32_t r[2][32];
@@ -920,6 +995,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
           }
         }
       }
+      }
       if (valid) {
         if (p.mode == kAnchorPass)
           p.lse_part[orow] = lse_own;
@@ -928,6 +1004,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       }
       it = nxt;
     }
+    // the output stores have read their staging buffers and written global memory
+    if (lane == 0) bulk_wait_group_all();
     tc_fence_before();
   }
 
@@ -972,12 +1050,13 @@ struct PairCfg {
   // j = 2 ic + qq, held in buffer j % kQBufs (its use j / kQBufs). A third or fourth
   // buffer (the next quad's queries loading a whole quad ahead, at the cost of a K/V
   // stage) measured no faster, nor did an L2 prefetch of the next quad's query rows.
-  static constexpr int kQBufs = 2;
+  static constexpr int kQBufs = 2;  // the query loader puts slot 2 ic + qq in buffer qq
   static constexpr int kStages = 4;
   static constexpr int kSmemQ = kQBufs * kQTileBytes;
   static constexpr int kSmemKV = kStages * kStageBytes;
-  static constexpr int kSmemBytes = kSmemQ + kSmemKV + 1024 + 1024;
+  static constexpr int kSmemBytes = kSmemQ + kSmemKV + 1024 + kSmemStage + 1024;
 };
+static_assert(PairCfg::kSmemBytes <= 232448, "shared memory of one CTA");
 
 struct Quad {
   int a_tok0, la, t0, ag;
@@ -1085,45 +1164,13 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
     }
     const uint64_t keep = l2_policy_evict_last(), stream_pol = l2_policy_evict_first();
     uint32_t kv_seq = 0, it_count = 0;
-    uint32_t q_arm[4] = {0, 0, 0, 0}, k_arm[4] = {0, 0, 0, 0}, v_arm[4] = {0, 0, 0, 0};
+    uint32_t k_arm[4] = {0, 0, 0, 0}, v_arm[4] = {0, 0, 0, 0};
     bool skip_pending = lead && p.inject_skip_first_kv != 0;
     bool ok = true;
-    // Queries: query tile qq of the quad with walk count ic is query slot 2 ic + qq. Slots
-    // are issued strictly in order; n_issued counts them.
-    uint32_t n_issued = 0;
-    auto issue_q = [&](const Quad& x) {
-      const int qq = static_cast<int>(n_issued & 1u);
-      const int buf = static_cast<int>(n_issued % C::kQBufs);
-      ++n_issued;
-      if (lead) ++q_arm[buf];
-      if (elect) {
-        if (lead) mbar_arrive_expect_tx(&bars->q_full[buf], 2 * C::kQTileBytes);
-        for (int kb = 0; kb < C::kKB; ++kb)
-          tma_load_3d_pair(&maps.q, lead_bar(&bars->q_full[buf]),
-                           sQ + buf * C::kQTileBytes + kb * C::kBlockBytes, kb * 64,
-                           (x.ag % hkv) * G, x.t0 + (2 * qq + static_cast<int>(rank)) * tok,
-                           stream_pol);
-      }
-      __syncwarp();
-    };
-    // Whether the buffer of query slot j = n_issued is free, polled (warp-uniform). The
-    // parity test is exact only because slot j - kQBufs, the buffer's previous use, has been
-    // issued (in-order issue): the buffer's empty barrier is then at most one phase short
-    // of the release that slot j needs, never two (two short, the same parity would read
-    // as released).
-    auto next_slot_free = [&]() {
-      const uint32_t j = n_issued;
-      const int buf = static_cast<int>(j % C::kQBufs);
-      const uint32_t par = ((j / C::kQBufs) & 1u) ^ 1u;
-      return __shfl_sync(0xFFFFFFFFu, mbar_test_wait(smem_u32(&bars->q_empty[buf]), par) ? 1 : 0,
-                         0) != 0;
-    };
     int item = first;
     Quad it = item < total_items ? load_quad(p, item) : Quad{};
     for (; ok && item < total_items; item += stride, ++it_count) {
-      const bool has_next = item + stride < total_items;
-      const Quad nxt = has_next ? load_quad(p, item + stride) : it;
-      const uint32_t cur_end = 2 * it_count + 2;  // one past this quad's query slots
+      const Quad nxt = item + stride < total_items ? load_quad(p, item + stride) : it;
       const int nA = it.n_anchor_tiles();
       const int n_tiles = it.n_tiles();
       const bool sh = it.sfx_shared();
@@ -1163,20 +1210,6 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
           }
           __syncwarp();
         }
-        if (pos == 0) {  // this quad's queries, unless they went out during the last quad
-          while (ok && n_issued < cur_end) {
-            const uint32_t j = n_issued;
-            const int buf = static_cast<int>(j % C::kQBufs);
-            if (!(ok = wait_parity_warp(wc, &bars->q_empty[buf], ((j / C::kQBufs) & 1u) ^ 1u)))
-              break;
-            issue_q(it);
-          }
-          if (!ok) break;
-        }
-        // the next quad's queries load while this one runs, as soon as their buffers are
-        // free (after this quad's own query slots, so in order)
-        while (has_next && n_issued < cur_end + 2 && n_issued >= cur_end && next_slot_free())
-          issue_q(nxt);
         if (!(ok = wait_parity_warp(wc, &bars->v_empty[slot], ph ^ 1u))) break;
         if (lead) ++v_arm[slot];
         if (elect) {
@@ -1192,12 +1225,45 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
     // (rank 1's loads complete on rank 0's barriers)
     if (lead) {
       const uint64_t dl = global_timer_ns() + 100000000ull;
-      for (int b = 0; b < C::kQBufs; ++b)
-        if (q_arm[b]) drain_wait(&bars->q_full[b], (q_arm[b] - 1) & 1u, dl);
       for (int s = 0; s < C::kStages; ++s) {
         if (k_arm[s]) drain_wait(&bars->k_full[s], (k_arm[s] - 1) & 1u, dl);
         if (v_arm[s]) drain_wait(&bars->v_full[s], (v_arm[s] - 1) & 1u, dl);
       }
+    }
+   } else if (warp == kWarpQLoad) {
+    // both CTAs: their query tiles. Query tile qq of the quad with walk count ic is query
+    // slot 2 ic + qq, in buffer qq; each loads as soon as its buffer is free (the commit
+    // after the previous quad's last S of that pair tile), apart from the K/V ring. The
+    // waits run in slot order, so a buffer's empty barrier is at most one phase short of
+    // the release a wait asks for.
+    const bool elect = elect_one();
+    const uint64_t stream_pol = l2_policy_evict_first();
+    uint32_t it_count = 0, q_arm[2] = {0, 0};
+    bool ok = true;
+    int item = first;
+    Quad it = item < total_items ? load_quad(p, item) : Quad{};
+    for (; ok && item < total_items; item += stride, ++it_count) {
+      const Quad nxt = item + stride < total_items ? load_quad(p, item + stride) : it;
+      for (int qq = 0; qq < 2 && ok; ++qq) {
+        if (!(ok = wait_parity_warp(wc, &bars->q_empty[qq], (it_count & 1u) ^ 1u))) break;
+        if (lead) ++q_arm[qq];
+        if (elect) {
+          if (lead) mbar_arrive_expect_tx(&bars->q_full[qq], 2 * C::kQTileBytes);
+          for (int kb = 0; kb < C::kKB; ++kb)
+            tma_load_3d_pair(&maps.q, lead_bar(&bars->q_full[qq]),
+                             sQ + qq * C::kQTileBytes + kb * C::kBlockBytes, kb * 64,
+                             (it.ag % hkv) * G, it.t0 + (2 * qq + static_cast<int>(rank)) * tok,
+                             stream_pol);
+        }
+        __syncwarp();
+      }
+      it = nxt;
+    }
+    // rank 0: every query load of the pair that was issued has landed before the CTAs exit
+    if (lead) {
+      const uint64_t dl = global_timer_ns() + 100000000ull;
+      for (int b = 0; b < 2; ++b)
+        if (q_arm[b]) drain_wait(&bars->q_full[b], (q_arm[b] - 1) & 1u, dl);
     }
    } else if (warp == kWarpFillCheck && lead) {
     // rank 0: the fill checker, as in the single-CTA kernel, on rank 0's full barriers
@@ -1341,6 +1407,8 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
     const uint32_t t_s = tmem + lane_base + 256u * q;
     const uint32_t t_o = t_s + 128u;
     const uint32_t p_full_lead = lead_bar(&bars->p_full[q]);
+    const uint32_t stage = smem_u32(smem + C::kSmemQ + C::kSmemKV + 1024) + warp * kStageWarpBytes;
+    const uint64_t out_pol = l2_policy_evict_first();
     uint32_t s_cnt = 0, it_count = 0;
     bool ok = true;
     const float c = p.scale_log2;
@@ -1441,6 +1509,10 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
       const uint64_t il = f2(inv_l, inv_l);
       const int64_t orow = static_cast<int64_t>(t) * p.hq + g * G + (row % G);
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + orow * D;
+      if (__all_sync(0xFFFFFFFFu, valid)) {
+        store_rows_tma<D>(&maps.out, t_o, il, stage, lane, g * G,
+                          it.t0 + j * tok + (warp & 3) * (32 / G), out_pol);
+      } else {
 #pragma unroll
       for (int ch2 = 0; ch2 < D / 64; ++ch2) {
         uint32_t r[2][32];
@@ -1465,11 +1537,13 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
           }
         }
       }
+      }
       if (valid && p.lse != nullptr)
         p.lse[orow] = (m_ref + __log2f(l)) * 0.69314718055994531f;
       it = nxt;
       in = nxt_in;
     }
+    if (lane == 0) bulk_wait_group_all();
     tc_fence_before();
   }
 

@@ -137,6 +137,9 @@ int64_t cascade_item_bound(int num_anchors, int64_t total_suffix_tokens, int hkv
 struct CascadeMaps {
   CUtensorMap q, k_anc, v_anc, k_suf, v_suf;
   CUtensorMap k_anc64, k_suf64;  // the same K tensors with 64-row boxes (CTA-pair halves)
+  // bf16 output [T_S, Hq, d] for the epilogue's TMA stores: box (32 of d, G heads, 32 / G
+  // tokens) = one warp's rows, 64-byte swizzle (fused mode only)
+  CUtensorMap out;
 };
 
 // Which d = 128 fused calls run the CTA-pair kernel: QUAIL_CTA_PAIRS_OFF / _AUTO (the
