@@ -219,11 +219,12 @@ __device__ __forceinline__ void st_global_v8(void* p, const uint32_t* v) {
 // Epilogue of one warp whose 32 rows are all valid output rows: O / l as bf16 through
 // shared memory and TMA tensor stores. The warp's TMEM lanes are 32 / G consecutive
 // tokens x G heads, which is one box (32 columns of d, G heads, 32 / G tokens) of the
-// output map. Each 32-column chunk (64 bytes a row, 2 KB the warp) goes to one of two
-// buffers with the 64-byte swizzle (16-byte chunk c of row r at c ^ ((r >> 1) & 3), so
-// each st.shared of the warp takes the minimum four wavefronts) and leaves by one TMA
-// store; a buffer is rewritten only once the store issued from it before has read it.
-// The per-thread 32-byte row stores this replaces touch 32 cache lines per instruction.
+// output map. Each 64-column half of the row (128 bytes a row) is staged as two 32-column
+// boxes in the warp's two 2 KB buffers with the 64-byte swizzle (16-byte chunk c of row r
+// at c ^ ((r >> 1) & 3), so each st.shared of the warp takes the minimum four wavefronts),
+// made visible to the async proxy by one fence and written by two TMA stores; the buffers
+// are rewritten only once the stores issued from them before have read them. The
+// per-thread 32-byte row stores this replaces touch 32 cache lines per warp instruction.
 template <int D>
 __device__ __forceinline__ void store_rows_tma(const CUtensorMap* map, uint32_t t_o, uint64_t il,
                                                uint32_t stage, int lane, int head0, int tok0,
@@ -237,6 +238,8 @@ __device__ __forceinline__ void store_rows_tma(const CUtensorMap* map, uint32_t 
     tmem_ld32(t_o + ch2 * 64 + 32, r[1]);
     tmem_wait_ld_dep(r[0]);
     reg_dep(r[1]);
+    if (lane == 0) bulk_wait_group_read<0>();
+    __syncwarp();
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       uint32_t pk[16];
@@ -247,19 +250,18 @@ __device__ __forceinline__ void store_rows_tma(const CUtensorMap* map, uint32_t 
                  lo, hi);
         pk[e] = pack_bf16(lo, hi);
       }
-      if (lane == 0) bulk_wait_group_read<1>();
-      __syncwarp();
-      const uint32_t buf = static_cast<uint32_t>(h) * 2048u;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        st_shared_v4(row_addr + buf + 16u * (static_cast<uint32_t>(c) ^ sw), pk[4 * c],
-                     pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_3d_hint(map, stage + buf, ch2 * 64 + h * 32, head0, tok0, policy);
-        bulk_commit_group();
-      }
+        st_shared_v4(row_addr + static_cast<uint32_t>(h) * 2048u +
+                         16u * (static_cast<uint32_t>(c) ^ sw),
+                     pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d_hint(map, stage, ch2 * 64, head0, tok0, policy);
+      tma_store_3d_hint(map, stage + 2048u, ch2 * 64 + 32, head0, tok0, policy);
+      bulk_commit_group();
     }
   }
 }
@@ -926,7 +928,7 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
       // This launch's partial: lse_own (natural log) and O / l. The suffix pass of the
       // two-pass variant may merge it with the anchor partial here (A4: LSE rescaling).
       const float lse_own = (m_used + __log2f(l)) * 0.69314718055994531f;
-      float w_own = 1.0f / l, w_part = 0.0f, lse_out = lse_own;
+      float w_own = __fdividef(1.0f, l), w_part = 0.0f, lse_out = lse_own;
       const float* part = nullptr;
       if (p.mode == kSuffixPass && p.merge && valid) {
         const float lse_a = __ldg(p.lse_part + orow);
@@ -1505,7 +1507,7 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
       __syncwarp();
       if (!(ok = wait_parity(wc, &bars->o_done[q], it_count & 1u))) break;
       tc_fence_after();
-      const float inv_l = 1.0f / l;
+      const float inv_l = __fdividef(1.0f, l);
       const uint64_t il = f2(inv_l, inv_l);
       const int64_t orow = static_cast<int64_t>(t) * p.hq + g * G + (row % G);
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + orow * D;
