@@ -61,6 +61,8 @@ def parse(argv=None):
                     help="fewer rows for --workload head (profiling only)")
     ap.add_argument("--suffixes-per-anchor", type=int, default=None,
                     help="smaller case of the same workload (profiling only)")
+    ap.add_argument("--sequences", type=int, default=None,
+                    help="fewer sequences for --workload prefill (profiling only)")
     return ap.parse_args(argv)
 
 
@@ -1122,6 +1124,8 @@ def run_prefill(args):
     stream = torch.cuda.current_stream()
     pk, src = peaks()
     cfg = workloads.ATTN_CONFIGS["prefill"]
+    if args.sequences:
+        cfg = dataclasses.replace(cfg, num_anchors=args.sequences)
     lay = workloads.make_layout(cfg)
     t = workloads.make_attention_inputs(cfg, lay, dev)
     hq, hkv, d = cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim
@@ -1156,8 +1160,9 @@ def run_prefill(args):
             "roofline": {"bound": "tensor", "achieved": round(tflops, 2),
                          "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(tflops / pk["bf16_tflops"], 4),
-                         "traffic": (None if pair_kernel(lay, hq, hkv, d) else
-                                     traffic_from_profile("cascade.cu", "cascade_attn_prefill.md")),
+                         "traffic": traffic_from_profile(
+                             "cascade.cu", "cascade_pair_prefill.md" if pair_kernel(lay, hq, hkv, d)
+                             else "cascade_attn_prefill.md"),
                          "peak_source": f"bf16_tflops (burst) of {src}",
                          "kernel": (("cascade_pair_kernel (CTA pairs)" if pair_kernel(lay, hq, hkv, d) else "cascade_attn_kernel") + " with anchors of length 0, one call"),
                          "algorithmic_flops_per_launch": flops},
