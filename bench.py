@@ -814,7 +814,7 @@ def run_e2e_chunked(q, cfg, layout, t, h_all, last, k_scale, v_scale, dev, strea
         logits_h[s0:s1].copy_(logits[:s1 - s0], non_blocking=True)
         am_h[s0:s1].copy_(am[:s1 - s0], non_blocking=True)
 
-    def run(n_steps):
+    def run(n_steps, step_ends=None):
         n = n_steps * len(plan)
         copy_stream.wait_stream(stream)
         copy_in(0)
@@ -822,17 +822,24 @@ def run_e2e_chunked(q, cfg, layout, t, h_all, last, k_scale, v_scale, dev, strea
             if i + 1 < n:
                 copy_in(i + 1)
             compute(i)
+            if step_ends is not None and (i + 1) % len(plan) == 0:
+                step_ends[i // len(plan)].record(stream)
 
     run(1)
     torch.cuda.synchronize()
     barrier(world)
     bw = h2d_bandwidth(dev)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a = torch.cuda.Event(enable_timing=True)
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     a.record(stream)
-    run(steps)
-    b.record(stream)
+    run(steps, ends)
     torch.cuda.synchronize()
-    ms = max_over_ranks(world, a.elapsed_time(b)) / steps
+    ms = max_over_ranks(world, a.elapsed_time(ends[-1])) / steps
+    step_ms = [round(a.elapsed_time(ends[0]), 1)] + [
+        round(ends[i - 1].elapsed_time(ends[i]), 1) for i in range(1, steps)]
+    # the same copy probe right after the timed steps: a lower rate here than before them
+    # means the host link was shared with other work during the leg
+    bw_after = h2d_bandwidth(dev)
     if q.get_device_error() != q.QUAIL_OK:
         raise RuntimeError("device error during the end-to-end run")
     del bufs, out, host, ws
@@ -844,11 +851,14 @@ def run_e2e_chunked(q, cfg, layout, t, h_all, last, k_scale, v_scale, dev, strea
             "ms_per_step": ms, "steps": steps, "anchor_groups": len(plan),
             "overlap": "inputs of anchor group i + 1 copied on a second stream while group i "
                        "computes",
+            "step_ms": step_ms,
             "roofline": {"bound": "host-to-device copy", "h2d_gbs_measured": round(bw, 1),
+                         "h2d_gbs_after": round(bw_after, 1),
                          "copy_bound_ms": round(copy_ms, 3),
                          "frac": round(copy_ms / ms, 4),
                          "how": "one pinned 1 GiB host-to-device copy (cudaMemcpyAsync), "
-                                "best of 5, same process"}}
+                                "best of 5, same process, before the timed steps (and "
+                                "after them: h2d_gbs_after)"}}
 
 
 def measure_softmax_stress(q, args, dev, scales=(4.0, 8.0)):

@@ -263,6 +263,7 @@ __device__ __forceinline__ void store_rows_tma(const CUtensorMap* map, uint32_t 
       tma_store_3d_hint(map, stage + 2048u, ch2 * 64 + 32, head0, tok0, policy);
       bulk_commit_group();
     }
+    __syncwarp();  // converged again before the next .sync.aligned tcgen05.ld
   }
 }
 
