@@ -31,13 +31,14 @@
 //      instance over the items the fast kernel listed
 //
 // Per CTA of the attention kernel:
-//   warp 8      TMA producer: Q tiles, then a ring of K / V tiles (128 keys each)
+//   warp 8      TMA producer: a ring of K / V tiles (128 keys each)
 //   warp 9      MMA issuer:   S_q = Q_q K^T (SMEM x SMEM -> TMEM), O_q += P_q V
 //                             (P from TMEM, V from SMEM), tcgen05 kind::f16, M = 128
 //   warp 10     fill checker: folds the V and next-K fills into the P-ready barrier
-//   warps 0-3   softmax of query tile 0, one thread per TMEM lane (= query row)
-//   warps 4-7   softmax of query tile 1
-//   warp 11     idle (it completes the third warpgroup for the register split)
+//   warp 11     query loader: each item's two query tiles, as soon as their buffers free
+//   warps 0-3   softmax of query tile 0, one thread per TMEM lane (= query row), and its
+//               epilogue (O / l through shared memory and TMA tensor stores)
+//   warps 4-7   softmax and epilogue of query tile 1
 // TMEM (512 columns): tile q uses S/P at columns 256q .. +127 and O at 256q+128 .. +255.
 // The two query tiles share every anchor KV tile loaded into shared memory and ping-pong:
 // while one warpgroup exponentiates its scores the tensor core works on the other tile.
@@ -1321,7 +1322,8 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
       const int nA = it.n_anchor_tiles();
       const int n = nA + it.n_sfx_tiles();
       const bool sh = it.sfx_shared();
-      // this quad's query buffers (query slots 2 it_count and 2 it_count + 1)
+      // this quad's query buffers (query slots 2 it_count and 2 it_count + 1, which the
+      // query-loader warp fills)
       auto qbuf = [&](int q) { return static_cast<int>((2 * it_count + q) % C::kQBufs); };
       auto quse = [&](int q) { return ((2 * it_count + q) / C::kQBufs) & 1u; };
       auto wait_s = [&](int q, int k) -> bool {
