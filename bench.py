@@ -624,7 +624,8 @@ def measure_attention(q, cfg, layout, dev, args, *, steps, e2e=False, cpu_budget
         # seconds of host-only work the copies ran ~10 % slower)
         res["e2e"] = run_e2e_chunked(q, cfg, layout, t, hx["h"], last, k_scale, v_scale, dev,
                                      stream, world, steps=max(3, min(steps, 6)),
-                                     host=e2e_host)
+                                     host=e2e_host, head_weights=(hx["gamma"], hx["w8"]),
+                                     check=(out, logits, am))
         del e2e_host
     parity_refs = {}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -711,7 +712,7 @@ def e2e_host_inputs(t, h_all, last, k_scale, v_scale):
 
 
 def run_e2e_chunked(q, cfg, layout, t, h_all, last, k_scale, v_scale, dev, stream, world,
-                    steps, n_chunks=8, host=None):
+                    steps, n_chunks=8, host=None, head_weights=None, check=None):
     """Same metric through the C ABI with host buffers. Every step copies all of its inputs
     from pinned host memory (queries, anchor and suffix K/V, offsets, the hidden states of
     the last tokens) and reads the step's result (logits and argmax) back. The batch goes
@@ -767,7 +768,10 @@ def run_e2e_chunked(q, cfg, layout, t, h_all, last, k_scale, v_scale, dev, strea
     out = torch.empty(max(max_ts, 1), hq, d, dtype=torch.bfloat16, device=dev)
     ws = torch.empty(mx(lambda p: p["ws"]), dtype=torch.uint8, device=dev)
     hcfg = workloads.HEAD_CONFIGS["join_last_token"]
-    gamma, w8 = (workloads.make_head_inputs(hcfg, dev, num_rows=1)[k] for k in ("gamma", "w8"))
+    if head_weights is not None:  # the device-resident step's RMSNorm gain and W8
+        gamma, w8 = head_weights
+    else:
+        gamma, w8 = (workloads.make_head_inputs(hcfg, dev, num_rows=1)[k] for k in ("gamma", "w8"))
     S = layout.num_suffixes
     logits = torch.empty(max(max_s, 1), 8, dtype=torch.float32, device=dev)
     am = torch.empty(max(max_s, 1), dtype=torch.int32, device=dev)
@@ -842,6 +846,17 @@ def run_e2e_chunked(q, cfg, layout, t, h_all, last, k_scale, v_scale, dev, strea
     bw_after = h2d_bandwidth(dev)
     if q.get_device_error() != q.QUAIL_OK:
         raise RuntimeError("device error during the end-to-end run")
+    # the results against the device-resident step's: every suffix's logits and argmax
+    # (read back each step), and the attention output of the last anchor group
+    agree = None
+    if check is not None:
+        out_full, logits_full, am_full = check
+        u0, u1 = plan[-1]["sr"]
+        attn = ((out[:u1 - u0].float() - out_full[u0:u1].float()).abs().max().item()
+                if u1 > u0 else 0.0)
+        agree = {"head_logits_argmax_identical": bool(torch.equal(logits_h, logits_full.cpu()) and
+                                                      torch.equal(am_h, am_full.cpu())),
+                 "last_group_attention_max_abs_diff": attn}
     del bufs, out, host, ws
     torch.cuda.empty_cache()
     copy_ms = h2d / (bw * 1e9) * 1e3
@@ -852,6 +867,7 @@ def run_e2e_chunked(q, cfg, layout, t, h_all, last, k_scale, v_scale, dev, strea
             "overlap": "inputs of anchor group i + 1 copied on a second stream while group i "
                        "computes",
             "step_ms": step_ms,
+            "vs_resident": agree,
             "roofline": {"bound": "host-to-device copy", "h2d_gbs_measured": round(bw, 1),
                          "h2d_gbs_after": round(bw_after, 1),
                          "copy_bound_ms": round(copy_ms, 3),
