@@ -627,7 +627,6 @@ def measure_attention(q, cfg, layout, dev, args, *, steps, e2e=False, cpu_budget
                                      host=e2e_host, head_weights=(hx["gamma"], hx["w8"]),
                                      check=(out, logits, am))
         del e2e_host
-        release_huge_pinned()
     parity_refs = {}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         def host_cases(ids):
@@ -688,57 +687,14 @@ def _chunks(layout, n):
     return [(cuts[i], cuts[i + 1]) for i in range(len(cuts) - 1)]
 
 
-_HUGE_PINNED = []  # (mmap, address) of host buffers registered with cudaHostRegister
-_HOST_PAGES = {"huge": 0, "default": 0}  # how the end-to-end leg's host inputs were pinned
-
-
-def pinned_huge(shape, dtype):
-    """A page-locked host tensor on transparent huge pages: anonymous memory advised with
-    MADV_HUGEPAGE, touched, then registered with cudaHostRegister (None if any step is
-    refused). Large sets of default pinned pages (tens of GB) fed the host-to-device
-    copies at half the rate of a 1 GiB buffer on some boxes; huge pages need far fewer
-    address translations for the copy engines."""
-    import ctypes
-    import mmap
-    nbytes = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
-    if nbytes == 0:
-        return None
-    try:
-        m = mmap.mmap(-1, nbytes, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
-        arr = np.frombuffer(m, dtype=np.uint8)
-        addr = arr.ctypes.data
-        libc = ctypes.CDLL("libc.so.6", use_errno=True)
-        if libc.madvise(ctypes.c_void_p(addr), ctypes.c_size_t(nbytes), 14) != 0:  # MADV_HUGEPAGE
-            return None
-        arr[::4096] = 0  # touch every page before it is locked
-        if int(torch.cuda.cudart().cudaHostRegister(addr, nbytes, 0)) != 0:
-            return None
-    except Exception:
-        return None
-    _HUGE_PINNED.append((m, addr))
-    return torch.from_numpy(arr).view(dtype).view(shape)
-
-
-def release_huge_pinned():
-    while _HUGE_PINNED:
-        m, addr = _HUGE_PINNED.pop()
-        torch.cuda.cudart().cudaHostUnregister(addr)
-
-
 def e2e_host_inputs(t, h_all, last, k_scale, v_scale):
     """The step's inputs in pinned host memory (queries, anchor and suffix K/V, the hidden
     states of the last tokens, FP8 scales), as a caller of the end-to-end path holds them.
     Made once, early in the process: pinned buffers made after much host allocation churn
     (a second or third 57 GB set in one process) fed the host-to-device copies at ~155
-    instead of ~210 GB/s on GB300. Huge-page pinned memory where the host allows it,
-    else torch's pinned allocator."""
+    instead of ~210 GB/s on GB300."""
     def pinned_like(x):
-        h = pinned_huge(tuple(x.shape), x.dtype)
-        if h is None:
-            _HOST_PAGES["default"] += 1
-            return torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-        _HOST_PAGES["huge"] += 1
-        return h
+        return torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
     names = ["q_suf", "k_anc", "v_anc", "k_suf", "v_suf"]
     host = {k: pinned_like(t[k]) for k in names}
     for k in names:
@@ -877,6 +833,25 @@ def run_e2e_chunked(q, cfg, layout, t, h_all, last, k_scale, v_scale, dev, strea
     torch.cuda.synchronize()
     barrier(world)
     bw = h2d_bandwidth(dev)
+    # the copy rate of the step's own pinned inputs, a group-sized slice at a time with
+    # nothing else running (min / median / max over the slices): the 1 GiB probe above
+    # stays at ~211 GB/s on every box, while on some boxes the leg's copies ran at half
+    # that or less
+    rates = []
+    for k in ("q_suf", "k_suf", "v_suf"):
+        for p_ in plan:
+            u0, u1 = p_["sr"]
+            if u1 <= u0:
+                continue
+            src, dstb = host[k][u0:u1], bufs[0][k][:u1 - u0]
+            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ea.record(stream)
+            dstb.copy_(src, non_blocking=True)
+            eb.record(stream)
+            torch.cuda.synchronize()
+            rates.append(src.numel() * src.element_size() / (ea.elapsed_time(eb) / 1e3) / 1e9)
+    set_rates = ({"min": round(min(rates), 1), "median": round(statistics.median(rates), 1),
+                  "max": round(max(rates), 1), "slices": len(rates)} if rates else None)
     a = torch.cuda.Event(enable_timing=True)
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     a.record(stream)
@@ -912,9 +887,7 @@ def run_e2e_chunked(q, cfg, layout, t, h_all, last, k_scale, v_scale, dev, strea
                        "computes",
             "step_ms": step_ms,
             "vs_resident": agree,
-            "host_buffers": ("pinned, transparent huge pages" if not _HOST_PAGES["default"]
-                             else "pinned (torch allocator)" if not _HOST_PAGES["huge"]
-                             else "pinned, partly on huge pages"),
+            "host_set_h2d_gbs": set_rates,
             "roofline": {"bound": "host-to-device copy", "h2d_gbs_measured": round(bw, 1),
                          "h2d_gbs_after": round(bw_after, 1),
                          "copy_bound_ms": round(copy_ms, 3),
