@@ -1361,7 +1361,16 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
         if ((k >= nA && !sh) || q == 1) mma_commit_pair(&bars->k_empty[slot]);
         if (k == n - 1) mma_commit_pair(&bars->q_empty[qbuf(q)]);
       };
-      auto mma_pv = [&](int q, int k) {
+      // 16-key steps of PV(q, k): keys past the last one that any row of pair tile q sees
+      // have P = 0 (the anchor's last tile; the last tile of the pair tile's suffix
+      // window), and their steps are left out
+      auto pv_steps = [&](int q, int k) {
+        const int vis = k < nA ? (k == nA - 1 ? it.la - k * kBN : kBN)
+                               : max(it.tend(2 * q), it.tend(2 * q + 1)) - it.wsp(q) -
+                                     (k - nA) * kBN;
+        return min(8, max(1, (vis + 15) / 16));
+      };
+      auto mma_pv = [&](int q, int k, int nkk) {
         const uint32_t seq = kv_base + pos_of(nA, sh, q, k);
         const int slot = seq % C::kStages;
         const uint32_t v_lo = v_lo0 + slot * (C::kStageBytes >> 4);
@@ -1370,8 +1379,9 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
         const uint32_t acc0 = k > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_pair_ts(d_o, a_p + 8u * kk, v_lo + kk * 128, kDescHi, kIdescPV,
-                      kk > 0 ? 1u : acc0);
+          if (kk < nkk)
+            mma_pair_ts(d_o, a_p + 8u * kk, v_lo + kk * 128, kDescHi, kIdescPV,
+                        kk > 0 ? 1u : acc0);
         if ((k >= nA && !sh) || q == 1) mma_commit_pair(&bars->v_empty[slot]);
         if (k == n - 1) mma_commit_pair(&bars->o_done[q]);
       };
@@ -1385,11 +1395,12 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
       }
       for (int k = 0; ok && k < n; ++k) {
         for (int q = 0; q < 2 && ok; ++q) {
+          const int nkk = pv_steps(q, k);
           ok = wait_pv(q);
           if (!ok) break;
           tc_fence_after();
           if (elect) {
-            mma_pv(q, k);
+            mma_pv(q, k, nkk);
             if (k + 1 < n) mma_s(q, k + 1);
           }
           __syncwarp();
