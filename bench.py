@@ -92,10 +92,9 @@ def attention_bytes(layout, hq, hkv, d, kv_bytes=2) -> float:
 
 def pair_kernel(layout, hq, hkv, d) -> bool:
     """Whether quail_cascade_attn's automatic choice runs the CTA-pair kernel for this
-    layout: d = 128 and some query tile's suffix window can exceed 64 keys (128 / G
-    tokens a tile + the longest suffix - 1 > 64); the rule the library states for
-    QUAIL_CTA_PAIRS_AUTO."""
-    return d == 128 and (128 // (hq // hkv)) + int(layout.max_suffix_len) - 1 > 64
+    layout: every head_dim-128 fused call (the rule the library states for
+    QUAIL_CTA_PAIRS_AUTO)."""
+    return d == 128
 
 
 def work_items(layout, hkv, group) -> int:

@@ -401,8 +401,9 @@ void quail_debug_inject(int32_t skip_first_kv_load);
  * kernel runs two query tiles on one SM, and loads a suffix window of at most 64 keys as
  * one 64-key tile where the pair always uses 128-key tiles.
  *   QUAIL_CTA_PAIRS_OFF     always the single-SM kernel
- *   QUAIL_CTA_PAIRS_AUTO    (default) the pair kernel unless every query tile's suffix
- *                           window fits in 64 keys: 128 / G + max_suffix_len - 1 <= 64
+ *   QUAIL_CTA_PAIRS_AUTO    (default) the pair kernel (measured faster on every shape
+ *                           tried, short suffix windows included), except with the
+ *                           fault-injection switch on
  *   QUAIL_CTA_PAIRS_ALWAYS  always the pair kernel
  * Both give the same results within rounding. Process-wide; set it between calls, not
  * while another thread is launching. Returns QUAIL_ERR_INVALID_ARG for another `mode`.

@@ -2070,18 +2070,16 @@ cudaError_t launch_cascade(const CascadeParams& params, const CascadeMaps& maps,
                            bool fp8, int num_sms, cudaStream_t stream) {
   // The CTA-pair kernel takes d = 128 calls with both parts fused and no K/V amax (with
   // the fault-injection switch on, only when forced: then its own timeout path runs, else
-  // the single-CTA kernel's). Automatic
-  // choice: a pair tile's suffix window spans two query tiles and is loaded as 128-key
-  // tiles, while the single-CTA kernel loads a window of at most 64 keys as one 64-key
-  // tile; when every query tile's window fits in 64 keys (tokens per tile + the longest
-  // suffix - 1 <= 64: short suffixes, many per tile) the pair would do more work on the
-  // suffix part than it saves, and the single-CTA kernel runs.
+  // the single-CTA kernel's). The automatic choice takes it for all of them: its pair
+  // tiles load a short suffix window as a 128-key tile where the single-CTA kernel loads
+  // 64 keys, but its PV stops at the window's last key and its anchor tiles move half the
+  // operand bytes per SM, and it measured faster on every shape tried (join with 4, 8 and
+  // 16 query heads per KV head and suffixes of 1 to 24 tokens included).
   CascadeParams p = params;
   const int mode = g_cta_pairs.load();
   bool pairs = mode != QUAIL_CTA_PAIRS_OFF && head_dim == 128 && p.mode == kFused &&
                p.k_amax == nullptr && num_sms >= 2 &&
                (p.inject_skip_first_kv == 0 || mode == QUAIL_CTA_PAIRS_ALWAYS);
-  if (mode == QUAIL_CTA_PAIRS_AUTO && p.tok_per_tile + p.max_suffix_len - 1 <= 64) pairs = false;
   // no resident pair of SMs (e.g. a partition of the GPU): the single-CTA kernel
   if (pairs && (fp8 ? pair_clusters<true>(num_sms, stream) : pair_clusters<false>(num_sms, stream)) <= 0)
     pairs = false;
