@@ -268,6 +268,52 @@ __device__ __forceinline__ void store_rows_tma(const CUtensorMap* map, uint32_t 
   }
 }
 
+// The same with all D columns staged (4 KB per 64 columns) before one proxy fence and the
+// stores: one wait, before the staging is written, for the previous item's stores to have
+// read it.
+template <int D>
+__device__ __forceinline__ void store_rows_tma_all(const CUtensorMap* map, uint32_t t_o,
+                                                   uint64_t il, uint32_t stage, int lane,
+                                                   int head0, int tok0, uint64_t policy) {
+  const uint32_t row_addr = stage + static_cast<uint32_t>(lane) * 64u;
+  const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+  if (lane == 0) bulk_wait_group_read<0>();
+  __syncwarp();
+#pragma unroll
+  for (int ch2 = 0; ch2 < D / 64; ++ch2) {
+    uint32_t r[2][32];
+    tmem_ld32(t_o + ch2 * 64, r[0]);
+    tmem_ld32(t_o + ch2 * 64 + 32, r[1]);
+    tmem_wait_ld_dep(r[0]);
+    reg_dep(r[1]);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        float lo, hi;
+        f2_split(f2_mul(f2(__uint_as_float(r[h][2 * e]), __uint_as_float(r[h][2 * e + 1])), il),
+                 lo, hi);
+        pk[e] = pack_bf16(lo, hi);
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        st_shared_v4(row_addr + static_cast<uint32_t>(ch2) * 4096u +
+                         static_cast<uint32_t>(h) * 2048u + 16u * (static_cast<uint32_t>(c) ^ sw),
+                     pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    }
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+#pragma unroll
+    for (int b = 0; b < 2 * (D / 64); ++b)
+      tma_store_3d_hint(map, stage + 2048u * b, 32 * b, head0, tok0, policy);
+    bulk_commit_group();
+  }
+  __syncwarp();  // converged again before the next .sync.aligned tcgen05.ld
+}
+
 // ---------------------------------------------------------------------------------
 // Softmax of one S tile: one thread per row, NC columns; P = 2^(s c - m) is written back
 // to TMEM as bf16 pairs (times pscale = v_scale on the anchor tiles of the FP8 variant)
@@ -1042,7 +1088,8 @@ cascade_attn_kernel(const __grid_constant__ CascadeParams p,
 // default CTA-scope semantics (no data moves through generic memory between the CTAs).
 // Suffix tiles always use N = 128 (a 64-key tile would split 32 / 32 between the CTAs, not
 // as the 64-row K halves are loaded).
-struct PairCfg {
+template <int STAGES>
+struct PairCfgT {
   static constexpr int kKB = 2;                          // 128-byte column blocks (d = 128)
   static constexpr int kBlockBytes = 128 * 128;          // 128 rows x 128 bytes
   static constexpr int kQTileBytes = 2 * kBlockBytes;    // one 128-row query tile
@@ -1055,12 +1102,18 @@ struct PairCfg {
   // buffer (the next quad's queries loading a whole quad ahead, at the cost of a K/V
   // stage) measured no faster, nor did an L2 prefetch of the next quad's query rows.
   static constexpr int kQBufs = 2;  // the query loader puts slot 2 ic + qq in buffer qq
-  static constexpr int kStages = 4;
+  // K/V ring depth: 4 stages, or 3 where the K/V stream is served from L2 (anchor K/V
+  // well inside L2, one suffix tile per pair tile); the 32 KB that frees doubles each
+  // softmax warp's epilogue staging, so all its output columns go out after one proxy
+  // fence instead of two halves in turn.
+  static constexpr int kStages = STAGES;
+  static constexpr int kStageWarpBytes = STAGES == 4 ? 2 * 2048 : 4 * 2048;
   static constexpr int kSmemQ = kQBufs * kQTileBytes;
   static constexpr int kSmemKV = kStages * kStageBytes;
-  static constexpr int kSmemBytes = kSmemQ + kSmemKV + 1024 + kSmemStage + 1024;
+  static constexpr int kSmemBytes = kSmemQ + kSmemKV + 1024 + 8 * kStageWarpBytes + 1024;
 };
-static_assert(PairCfg::kSmemBytes <= 232448, "shared memory of one CTA");
+static_assert(PairCfgT<4>::kSmemBytes <= 232448 && PairCfgT<3>::kSmemBytes <= 232448,
+              "shared memory of one CTA");
 
 struct Quad {
   int a_tok0, la, t0, ag;
@@ -1092,11 +1145,11 @@ __device__ __forceinline__ Quad load_quad(const CascadeParams& p, int item) {
   return it;
 }
 
-template <bool FP8>
+template <bool FP8, int STAGES>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 cascade_pair_kernel(const __grid_constant__ CascadeParams p,
                     const __grid_constant__ CascadeMaps maps) {
-  using C = PairCfg;
+  using C = PairCfgT<STAGES>;
   constexpr int D = 128;
   const int total_items = __ldg(p.prefix + p.num_anchors);  // quads
   extern __shared__ uint8_t smem_raw[];
@@ -1423,7 +1476,7 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
     const uint32_t t_s = tmem + lane_base + 256u * q;
     const uint32_t t_o = t_s + 128u;
     const uint32_t p_full_lead = lead_bar(&bars->p_full[q]);
-    const uint32_t stage = smem_u32(smem + C::kSmemQ + C::kSmemKV + 1024) + warp * kStageWarpBytes;
+    const uint32_t stage = smem_u32(smem + C::kSmemQ + C::kSmemKV + 1024) + warp * C::kStageWarpBytes;
     const uint64_t out_pol = l2_policy_evict_first();
     uint32_t s_cnt = 0, it_count = 0;
     bool ok = true;
@@ -1526,8 +1579,12 @@ cascade_pair_kernel(const __grid_constant__ CascadeParams p,
       const int64_t orow = static_cast<int64_t>(t) * p.hq + g * G + (row % G);
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + orow * D;
       if (__all_sync(0xFFFFFFFFu, valid)) {
-        store_rows_tma<D>(&maps.out, t_o, il, stage, lane, g * G,
-                          it.t0 + j * tok + (warp & 3) * (32 / G), out_pol);
+        if constexpr (C::kStageWarpBytes >= 2 * 2048 * (D / 64))
+          store_rows_tma_all<D>(&maps.out, t_o, il, stage, lane, g * G,
+                                it.t0 + j * tok + (warp & 3) * (32 / G), out_pol);
+        else
+          store_rows_tma<D>(&maps.out, t_o, il, stage, lane, g * G,
+                            it.t0 + j * tok + (warp & 3) * (32 / G), out_pol);
       } else {
 #pragma unroll
       for (int ch2 = 0; ch2 < D / 64; ++ch2) {
@@ -1991,15 +2048,16 @@ static cudaError_t launch_attn_kernel(const CascadeParams& p, const CascadeMaps&
 }
 
 // Clusters of two CTAs (one per SM) that can be resident at once, per device.
-template <bool FP8>
+template <bool FP8, int STAGES>
 static int pair_clusters(int num_sms, cudaStream_t stream) {
   static std::atomic<int> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   std::atomic<int>* slot = dev >= 0 && dev < 64 ? &cache[dev] : nullptr;
   if (slot != nullptr && slot->load() > 0) return slot->load();
-  if (cudaFuncSetAttribute(cascade_pair_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           PairCfg::kSmemBytes) != cudaSuccess) {
+  if (cudaFuncSetAttribute(cascade_pair_kernel<FP8, STAGES>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           PairCfgT<STAGES>::kSmemBytes) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -2007,9 +2065,10 @@ static int pair_clusters(int num_sms, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(num_sms / 2 * 2), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = PairCfg::kSmemBytes;
+  cfg.dynamicSmemBytes = PairCfgT<STAGES>::kSmemBytes;
   cfg.stream = stream;
-  if (cudaOccupancyMaxActiveClusters(&clusters, cascade_pair_kernel<FP8>, &cfg) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveClusters(&clusters, cascade_pair_kernel<FP8, STAGES>, &cfg) !=
+          cudaSuccess ||
       clusters <= 0) {
     cudaGetLastError();
     return 0;
@@ -2018,25 +2077,38 @@ static int pair_clusters(int num_sms, cudaStream_t stream) {
   return clusters;
 }
 
-template <bool FP8>
+template <bool FP8, int STAGES>
 static cudaError_t launch_pair_kernel(const CascadeParams& p, const CascadeMaps& maps,
                                       int num_sms, cudaStream_t stream) {
   cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, cascade_pair_kernel<FP8>);
+  cudaError_t e = cudaFuncGetAttributes(&attr, cascade_pair_kernel<FP8, STAGES>);
   if (e != cudaSuccess) return e;
   if (static_cast<int64_t>(attr.numRegs) * kThreads <
       256 * Cfg<128>::kRegsSoftmax + 128 * Cfg<128>::kRegsOther)
     return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(cascade_pair_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           PairCfg::kSmemBytes);
+  e = cudaFuncSetAttribute(cascade_pair_kernel<FP8, STAGES>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           PairCfgT<STAGES>::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int clusters = pair_clusters<FP8>(num_sms, stream);
+  const int clusters = pair_clusters<FP8, STAGES>(num_sms, stream);
   if (clusters <= 0) return cudaErrorInvalidConfiguration;
   // quads <= item_bound (the bound on two-tile items)
   const int grid = 2 * (p.item_bound < clusters ? p.item_bound : clusters);
   if (grid <= 0) return cudaSuccess;
-  cascade_pair_kernel<FP8><<<grid, kThreads, PairCfg::kSmemBytes, stream>>>(p, maps);
+  cascade_pair_kernel<FP8, STAGES><<<grid, kThreads, PairCfgT<STAGES>::kSmemBytes, stream>>>(p, maps);
   return cudaGetLastError();
+}
+
+// Ring depth of the pair kernel: 3 K/V stages (and all output columns staged at once) when
+// the anchor K/V is well inside L2 (<= 64 MB, K and V in bf16, so that every quad of an
+// anchor finds its tiles there) and each pair tile's suffix window is one 128-key tile (2
+// tokens-per-tile + the longest suffix - 1 <= 128 keys); else 4. Measured: join (33.6 MB
+// of anchor K/V, windows of at most 87 keys) 2-3 % faster with 3; ragged, fp8_long and
+// the causal prefill (anchor K/V or windows beyond that) unchanged or slower.
+static bool pair_shallow_ring(const CascadeParams& p) {
+  const int64_t anchor_kv_bytes = p.total_anchor_tokens * p.hkv * 128 * 2 * 2;
+  return anchor_kv_bytes <= (int64_t{64} << 20) &&
+         2 * p.tok_per_tile + p.max_suffix_len - 1 <= 128;
 }
 
 // The fast kernel (single CTAs, or CTA pairs over quads), then the exact kernel over the
@@ -2048,7 +2120,8 @@ static cudaError_t launch_attn_d(const CascadeParams& p, const CascadeMaps& maps
   const bool amax = !FP8 && p.k_amax != nullptr;
   cudaError_t e;
   if (D == 128 && p.tiles_per_item == 4)
-    e = launch_pair_kernel<FP8>(p, maps, num_sms, stream);
+    e = pair_shallow_ring(p) ? launch_pair_kernel<FP8, 3>(p, maps, num_sms, stream)
+                             : launch_pair_kernel<FP8, 4>(p, maps, num_sms, stream);
   else
     e = amax ? launch_attn_kernel<D, false, false, true>(p, maps, num_sms, stream)
              : launch_attn_kernel<D, FP8, false>(p, maps, num_sms, stream);
@@ -2081,7 +2154,8 @@ cudaError_t launch_cascade(const CascadeParams& params, const CascadeMaps& maps,
                p.k_amax == nullptr && num_sms >= 2 &&
                (p.inject_skip_first_kv == 0 || mode == QUAIL_CTA_PAIRS_ALWAYS);
   // no resident pair of SMs (e.g. a partition of the GPU): the single-CTA kernel
-  if (pairs && (fp8 ? pair_clusters<true>(num_sms, stream) : pair_clusters<false>(num_sms, stream)) <= 0)
+  if (pairs && (fp8 ? pair_clusters<true, 4>(num_sms, stream)
+                    : pair_clusters<false, 4>(num_sms, stream)) <= 0)
     pairs = false;
   p.tiles_per_item = pairs ? 4 : 2;
   cudaError_t e = cudaMemsetAsync(p.flag, 0, sizeof(int32_t), stream);
