@@ -26,8 +26,8 @@
 //   5. anchor_e4m3_to_bf16_kernel (grid, FP8 anchor KV only) stages the anchor codes as
 //                                        bf16 in the workspace
 //   6. the fast kernel - cascade_attn_kernel (persistent, one CTA per SM) or, for d = 128
-//      with suffix windows beyond 64 keys, cascade_pair_kernel (persistent clusters of two
-//      CTAs, 256-row tcgen05 MMAs over an SM pair) - then cascade_attn_kernel's exact
+//      fused calls, cascade_pair_kernel (persistent clusters of two CTAs, 256-row tcgen05
+//      MMAs over an SM pair, a 3- or 4-stage K/V ring) - then cascade_attn_kernel's exact
 //      instance over the items the fast kernel listed
 //
 // Per CTA of the attention kernel:
