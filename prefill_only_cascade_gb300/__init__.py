@@ -374,7 +374,7 @@ CTA_PAIRS_OFF, CTA_PAIRS_AUTO, CTA_PAIRS_ALWAYS = 0, 1, 2
 
 def set_cta_pairs(mode: int) -> int:
     """head_dim 128 kernel choice: CTA_PAIRS_OFF (single-SM kernel), CTA_PAIRS_AUTO (the
-    default: SM pairs unless every query tile's suffix window fits in 64 keys) or
+    default: SM pairs for every fused call, except with the fault-injection switch on) or
     CTA_PAIRS_ALWAYS. Returns the status."""
     return lib.quail_set_cta_pairs(int(mode))
 
