@@ -5,10 +5,12 @@ arrays of quail_cascade_attn) it gives
   * the algorithmic work - FLOPs of the visible (query, key) pairs, 4 d Hq sum_s sum_i
     (L_a + i + 1), and the bytes that must move (Q, out, lse, suffix K/V, anchor K/V once,
     offsets) - and the speed-of-light time max(FLOPs / tensor peak, bytes / HBM peak);
-  * a model of the library's kernel: the work items its schedule builds (anchor, KV head,
-    two 128-row query tiles), each costed in tensor-core cycles from measured single-CTA
-    tcgen05.mma rates, plus the steady-state efficiency and the per-item overhead measured
-    by a clock64 trace of the kernel, split over the persistent CTAs in the kernel's order.
+  * a model of the library's single-CTA kernel: the work items its schedule builds
+    (anchor, KV head, two 128-row query tiles), each costed in tensor-core cycles from
+    measured single-CTA tcgen05.mma rates, plus the steady-state efficiency and the
+    per-item overhead measured by a clock64 trace of the kernel, split over the persistent
+    CTAs in the kernel's order. For head_dim 128 the library runs the CTA-pair kernel,
+    which measures 3-6 % below this model (it moves half the operand bytes per SM).
 
 The method it models: "Motor de inferência Quail atinge 1 bilhão de tokens por minuto por
 GPU", section "Como funciona" (simplified cascade attention over a shared anchor and its
