@@ -2103,7 +2103,7 @@ static cudaError_t launch_pair_kernel(const CascadeParams& p, const CascadeMaps&
 // the anchor K/V is well inside L2 (<= 64 MB, K and V in bf16, so that every quad of an
 // anchor finds its tiles there) and each pair tile's suffix window is one 128-key tile (2
 // tokens-per-tile + the longest suffix - 1 <= 128 keys); else 4. Measured: join (33.6 MB
-// of anchor K/V, windows of at most 87 keys) 2-3 % faster with 3; ragged, fp8_long and
+// of anchor K/V, windows of at most 87 keys) 1-3 % faster with 3; ragged, fp8_long and
 // the causal prefill (anchor K/V or windows beyond that) unchanged or slower.
 static bool pair_shallow_ring(const CascadeParams& p) {
   const int64_t anchor_kv_bytes = p.total_anchor_tokens * p.hkv * 128 * 2 * 2;
